@@ -1,0 +1,422 @@
+"""Benchmark: skinny BF16 decode projection on GB300.
+
+Workload (default): the decode projection W[3584, 7168] bf16, one sweep of
+M = 1, 2, 4, 8, 16, 32 tokens per step (six projections, bf16 output), inputs
+resident in HBM.  Each projection reads a different copy of the weight from a
+rotation of R copies whose total is >= 2x the L2 size, so every weight read
+comes from HBM.  Prints one JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun each rank runs an independent replica on its own GPU (the
+projection has no exchange step); the step time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "us per projection and weight-stream HBM GB/s (% of GB300 peak) at M=1..64"
+N_DEC, K_DEC = 3584, 7168
+SWEEP = (1, 2, 4, 8, 16, 32)
+
+
+# ----------------------------------------------------------------------------- helpers
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    csrc = os.path.join(ROOT, "skinny_bf16_projection_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str) -> float | None:
+    """DRAM bytes per launch from the committed ncu summary, if the kernel sources
+    are unchanged since it was taken (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = kernel_source_hash()
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and parts[0] == workload and parts[1] == want:
+                return float(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms while running."""
+
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.rows: list[list[str]] = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9 and (self.uuid is None or self.uuid in parts[0]):
+                self.rows.append(parts)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        rows = self.rows
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+        busy = [r for r in rows if (num(r[4]) or 0) > 0] or rows
+        sm = [num(r[1]) for r in busy if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in busy for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(busy[0][2]), "reasons": reasons, "samples": len(busy)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo", rank=rank, world_size=world)
+    return rank, world, local
+
+
+def reduce_max(value: float, world: int) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+def oracle_step_rate(seconds: float, sweep=SWEEP, N=N_DEC, K=K_DEC):
+    """Time the oracle (as it stands) on the host cores over the same workload:
+    repeat full sweeps of the projection until `seconds` have elapsed (>= 1 sweep;
+    a sweep larger than ~30 s is cut to a row sample and scaled by N / rows).
+    Returns (weight GB/s, cores, sample description, seconds per sweep)."""
+    import oracle
+    import projection_inputs as pin
+    w, x = pin.case(N, K, seed=0)
+    cores = oracle.max_threads()
+    rows = N
+    t0 = time.perf_counter()
+    oracle.projection(x[:max(sweep)], w[:64], with_scale=False)  # warm + probe
+    probe = time.perf_counter() - t0
+    est_sweep = probe * (N / 64) * (sum(sweep) / max(sweep))
+    if est_sweep > 30.0:
+        rows = max(64, int(N * 30.0 / est_sweep))
+    ws = w[:rows]
+    sweeps = 0
+    t0 = time.perf_counter()
+    while True:
+        for M in sweep:
+            oracle.projection(x[:M], ws, with_scale=False)
+        sweeps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or el * (sweeps + 1) / sweeps > 3 * seconds:
+            break
+    per_sweep = el / sweeps * (N / rows)
+    gbs = len(sweep) * N * K * 2 / per_sweep / 1e9
+    sample = (f"{sweeps} full sweep(s) of M={list(sweep)} over W[{rows}/{N}, {K}] "
+              f"({el:.1f} s, fp64 oracle, {cores} threads)")
+    return gbs, cores, sample, per_sweep
+
+
+# ----------------------------------------------------------------------------- reference arm
+def reference_arm(args, rank, world):
+    """The oracle timed as it stands on the host cores.  One step = one sweep of
+    M = 1..32 over a row sample of the weight, sized so that warm-up + K steps
+    take about 90 s; throughput is scaled to weight bytes (rows * K * 2 per
+    projection)."""
+    if rank != 0:
+        return 0
+    import oracle
+    import projection_inputs as pin
+    oracle.build()
+    w, x = pin.case(N_DEC, K_DEC, seed=0)
+    cores = oracle.max_threads()
+    t0 = time.perf_counter()
+    for M in SWEEP:
+        oracle.projection(x[:M], w[:256], with_scale=False)
+    per_row = (time.perf_counter() - t0) / 256
+    budget = 90.0 / max(1, args.steps + args.warmup)
+    rows = int(max(8, min(N_DEC, budget / max(per_row, 1e-9))))
+    nblk = max(1, N_DEC // rows)
+
+    def one_step(i):
+        r0 = (i % nblk) * rows
+        ws = w[r0:r0 + rows]
+        t = time.perf_counter()
+        for M in SWEEP:
+            oracle.projection(x[:M], ws, with_scale=False)
+        return time.perf_counter() - t
+
+    for i in range(args.warmup):
+        one_step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        one_step(i)
+    el = time.perf_counter() - t0
+    per_step = el / args.steps
+    value = len(SWEEP) * rows * K_DEC * 2 / per_step / 1e9
+    sample = (f"each step: one sweep M={list(SWEEP)} over a {rows}-row slice of W[{N_DEC},{K_DEC}] "
+              f"(fp64 oracle, {cores} threads); {args.steps} steps in {el:.1f} s")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(per_step * 1e3 * N_DEC / rows, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded randn, bf16 inputs)",
+        "config": {"workload": f"decode projection W[{N_DEC},{K_DEC}] bf16, sweep M={list(SWEEP)} "
+                               f"(6 projections per step), bf16 out",
+                   "N": N_DEC, "K": K_DEC, "M": list(SWEEP), "out": "bf16",
+                   "parallelism": "replicas"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- our arm
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-tune", action="store_true", help="use the default plan")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        return reference_arm(args, rank, world)
+
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import projection_inputs as pin
+    import skinny_bf16_projection_gb300 as skg
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 128 << 20))
+    wbytes = N_DEC * K_DEC * 2
+    R = max(2, math.ceil(2 * l2 / wbytes))
+
+    w, x = pin.case(N_DEC, K_DEC, seed=0)
+    wd = w.to(dev)
+    weights = [wd] + [wd.clone() for _ in range(R - 1)]
+    projs = [skg.Projection(wc) for wc in weights]
+    if not args.no_tune:
+        projs[0].autotune(list(SWEEP))
+    plan = {M: projs[0].plan(M) for M in SWEEP}
+    for p in projs[1:]:
+        for M in SWEEP:
+            p.set_tactic(M, plan[M])
+    xd = x.to(dev)
+    xs = {M: xd[:M].contiguous() for M in SWEEP}
+    outs = {M: torch.empty((M, N_DEC), dtype=torch.bfloat16, device=dev) for M in SWEEP}
+    stream = torch.cuda.current_stream(dev)
+    launches_per_step = len(SWEEP)
+
+    # Each step is 6 launches; launch L reads weight copy L % R.  Steps are
+    # captured in CUDA graphs of G steps (6G % R == 0, so every graph starts at
+    # copy 0) and replayed; a remainder graph makes the count exactly K steps.
+    G = R * max(1, math.ceil(48 / R))
+
+    def capture(n_steps: int, fn):
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.graph(g, stream=side):
+            fn(n_steps)
+        stream.wait_stream(side)
+        return g
+
+    def sweep_steps(n_steps: int):
+        c = 0
+        for _ in range(n_steps):
+            for M in SWEEP:
+                projs[c % R].run(xs[M], outs[M])
+                c += 1
+
+    g_main = capture(G, sweep_steps)
+    rem = args.steps % G
+    g_rem = capture(rem, sweep_steps) if rem else None
+
+    # ---------------- timed region: exactly K steps, events on the launching stream
+    sampler = ClockSampler(getattr(props, "uuid", None) and str(props.uuid))
+    sampler.start()
+    time.sleep(0.3)
+    for _ in range(max(1, math.ceil(args.warmup / G))):
+        g_main.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps // G):
+        g_main.replay()
+    if g_rem is not None:
+        g_rem.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms_total = ev0.elapsed_time(ev1)
+    clocks = sampler.stop()
+    for p in projs:
+        p.check_status()
+    ms_total = reduce_max(ms_total, world)
+    ms_step = ms_total / args.steps
+    value = world * launches_per_step * wbytes / (ms_step * 1e-3) / 1e9  # weight GB/s, all ranks
+
+    # ---------------- per-M projection time (graph of 6R launches of one M, rotated)
+    per_m = {}
+    for M in SWEEP:
+        def one_m(n, M=M):
+            for i in range(n):
+                projs[i % R].run(xs[M], outs[M])
+        gm = capture(6 * R * 4, one_m)
+        gm.replay()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 20
+        a.record(stream)
+        for _ in range(reps):
+            gm.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / (reps * 6 * R * 4)
+        per_m[str(M)] = {"us": round(us, 3), "weight_GBps": round(wbytes / us / 1e3, 1),
+                         "tactic": plan[M]}
+        del gm
+
+    # ---------------- end to end: C-ABI call with pinned host buffers, copies inside
+    xh = {M: x[:M].contiguous().pin_memory() for M in SWEEP}
+    oh = {M: torch.empty((M, N_DEC), dtype=torch.bfloat16).pin_memory() for M in SWEEP}
+    e2e_steps = 200
+    for M in SWEEP:
+        projs[0].run_host(xh[M], oh[M])
+    barrier(world)
+    t0 = time.perf_counter()
+    c = 0
+    for _ in range(e2e_steps):
+        for M in SWEEP:
+            projs[c % R].run_host(xh[M], oh[M])
+            c += 1
+    e2e_s = reduce_max(time.perf_counter() - t0, world) / e2e_steps
+    e2e_value = world * launches_per_step * wbytes / e2e_s / 1e9
+
+    # ---------------- roofline of the projection kernel (the only kernel in the step)
+    peaks = measured_peaks()
+    alg_bytes = sum(wbytes + M * K_DEC * 2 + M * N_DEC * 2 for M in SWEEP) / len(SWEEP)
+    avg_launch_s = ms_step * 1e-3 / launches_per_step
+    achieved = alg_bytes / avg_launch_s / 1e9
+    traffic = recorded_traffic("decode_3584x7168_sweep")
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded randn, bf16 inputs, random weights)",
+        "config": {"workload": f"decode projection W[{N_DEC},{K_DEC}] bf16, sweep M={list(SWEEP)} "
+                               f"(6 projections per step), bf16 out",
+                   "N": N_DEC, "K": K_DEC, "M": list(SWEEP), "out": "bf16",
+                   "l2": f"rotating {R} weight copies ({R * wbytes / 1e6:.0f} MB >= 2x L2 "
+                         f"{l2 / 1e6:.0f} MB): every weight read comes from HBM",
+                   "parallelism": f"replicas x{world}"},
+        "us_per_projection": round(ms_step * 1e3 / launches_per_step, 3),
+        "per_M": per_m,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs, burst copy)",
+                     "traffic": traffic},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": sum(M * K_DEC * 2 for M in SWEEP),
+                "d2h_bytes_per_step": sum(M * N_DEC * 2 for M in SWEEP)},
+        "gpu_launches": args.steps * launches_per_step,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gbs, cores, sample, _ = oracle_step_rate(args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores,
+                                "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    barrier(world)
+    for p in projs:
+        p.close()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

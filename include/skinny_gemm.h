@@ -1,0 +1,193 @@
+/*
+ * skinny_gemm.h — C ABI of the GB300 (sm_103a) skinny BF16 decode projection.
+ *
+ *   out[M, N] = x[M, K] @ W[N, K]^T,   1 <= M <= 64 tokens,
+ *   x and W bf16, accumulation fp32, out bf16 (round to nearest even) or fp32.
+ *
+ * Operation: page "vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.
+ * gemm.warp_splitk", class PreparedWarpSplitK docstring (out[M, N] = x[M, K]
+ * @ weight[N, K]^T, x and out packed row-major, 32 B aligned); page
+ * "vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.gemm.projection",
+ * class PreparedProjection (prepare once, then run(x, out) into a
+ * caller-owned out; BF16 or FP32 output).
+ *
+ * Conventions for every entry point:
+ *   - Pointers named W, x, out, fa, out_* are DEVICE pointers on the current
+ *     CUDA device; pointers named *_host are HOST pointers.  Sizes are in
+ *     elements unless the name ends in _bytes.  Matrices are row-major with a
+ *     unit inner stride; ld* is the row pitch in elements.
+ *   - A stream argument is a cudaStream_t passed as void* (NULL = the legacy
+ *     default stream).  Events are cudaEvent_t passed as void*.
+ *   - Functions returning int return SKG_OK (0) or one of the codes below;
+ *     skinny_gemm_last_error() then describes the failure (thread-local
+ *     string, valid until the next call on the same thread).
+ *   - Nothing here allocates, synchronizes or copies between host and device
+ *     except where a function says so.
+ */
+#ifndef SKINNY_GEMM_H_
+#define SKINNY_GEMM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SKINNY_GEMM_ABI_VERSION 1
+#define SKINNY_GEMM_MAX_M 64
+
+typedef struct skinny_gemm_plan* skinny_gemm_t; /* opaque prepared projection */
+
+/* Element types.  W and x: SKG_BF16 (or SKG_FP16, both operands the same).
+ * out: SKG_BF16 or SKG_FP32 (projection page, PreparedProjection: "BF16/FP16
+ * [N, K]" weights, output dtype BF16 or FP32). */
+enum skinny_gemm_dtype { SKG_BF16 = 0, SKG_FP16 = 1, SKG_FP32 = 2 };
+
+/* Return codes.  The pages raise ValueError for the EINVAL/EALIGN cases
+ * (warp_splitk page, PreparedWarpSplitK.__init__; projection page,
+ * PreparedProjection.__init__ and .run) and fall back (None) where a token
+ * count has no kernel (low_latency_gemm page, select_kimi_k3_backend). */
+enum skinny_gemm_status {
+  SKG_OK = 0,
+  SKG_EINVAL = 1,          /* bad handle, shape, pitch or dtype */
+  SKG_EALIGN = 2,          /* pointer or row pitch not 16-byte aligned */
+  SKG_EUNSUPPORTED_M = 3,  /* M outside 1..64: caller falls back */
+  SKG_EDEVICE = 4,         /* current device is not sm_103 */
+  SKG_ECUDA = 5,           /* a CUDA runtime/driver call failed */
+  SKG_ECAPTURING = 6,      /* prepare/autotune called while the stream captures */
+  SKG_ETIMEOUT = 7         /* a device-side bounded wait expired (watchdog) */
+};
+
+/* Flags for skinny_gemm_prepare_ex. */
+#define SKG_PREPARE_NO_TUNE_CACHE 0x1u /* ignore SKINNY_GEMM_TACTIC_FILE */
+
+/*
+ * Prepare a projection for weight W[N, K] (packed, row pitch K).
+ * Validates W, encodes its TMA maps (box {64, rows}, 128-byte swizzle,
+ * 256-byte L2 promotion, out-of-bounds zero fill; projection page,
+ * weight_map) and builds the {M: tactic} plan for M = 1..64 (low_latency_gemm
+ * page, module docstring: the static part of the choice is resolved once, the
+ * per-call path is one lookup).  A tactic for M is the one of the smallest
+ * token tile >= M (glm5next gemm page, Projection.__init__).
+ *
+ * W is BORROWED: the handle stores its address; W must stay allocated and
+ * must not move while the handle lives (its contents may change between
+ * runs).  Requirements: N >= 1, K >= 8, K % 8 == 0, W 16-byte aligned.
+ * Allocates a small device status word (the watchdog).  Must not be called
+ * while a stream on this device is capturing (returns NULL, ECAPTURING).
+ * Returns NULL on error (see skinny_gemm_last_error / skinny_gemm_last_status).
+ */
+skinny_gemm_t skinny_gemm_prepare(const void* W, int64_t N, int64_t K, int dtype, int out_dtype);
+
+/* As skinny_gemm_prepare with an explicit row pitch ldw >= K (ldw % 8 == 0),
+ * so a row slice or column slice of a larger weight can be prepared in place
+ * (projection page, weight_map: "row pitch kept").  flags: SKG_PREPARE_*. */
+skinny_gemm_t skinny_gemm_prepare_ex(const void* W, int64_t N, int64_t K, int64_t ldw,
+                                     int dtype, int out_dtype, unsigned flags);
+
+/*
+ * out[M, N] = x[M, K] @ W^T on `stream`: one kernel launch, no allocation,
+ * no synchronization, no host<->device copy, so it can be captured in a CUDA
+ * graph.  x: device [M, K] packed (pitch K), 16-byte aligned.  out: device
+ * [M, N] packed (pitch N), 16-byte aligned base, in the prepared output dtype,
+ * caller-owned (projection page, PreparedProjection.run writes into out and
+ * returns it).  Rows >= M of x are never read and rows >= M of out are never
+ * written.  The launch carries programmatic dependent launch: the weight's
+ * first tiles are fetched before the kernel waits for the previous kernel on
+ * the stream (warp_splitk page, module docstring).
+ * Errors: EINVAL (bad handle/pointers), EUNSUPPORTED_M, EALIGN, ECUDA.
+ */
+int skinny_gemm_run(skinny_gemm_t h, const void* x, int64_t M, void* out, void* stream);
+
+/* As skinny_gemm_run with row pitches: x rows ldx >= K apart (ldx % 8 == 0,
+ * since x is read by TMA), out rows ldo >= N apart (any pitch; out is written
+ * with plain stores).  Used to feed a column slice of one output to the next
+ * projection. */
+int skinny_gemm_run_strided(skinny_gemm_t h, const void* x, int64_t ldx, int64_t M,
+                            void* out, int64_t ldo, void* stream);
+
+/*
+ * End-to-end call with HOST buffers: copies x_host [M, K] (pinned host memory
+ * gives an asynchronous copy) into a device staging buffer owned by the
+ * handle, runs the projection, copies the result into out_host [M, N] and
+ * synchronizes `stream` before returning.  The staging buffers are allocated
+ * on the first call (not capturable).  Calls on one handle must not overlap.
+ */
+int skinny_gemm_run_host(skinny_gemm_t h, const void* x_host, int64_t M, void* out_host,
+                         void* stream);
+
+/*
+ * The two-stream decode step (low_latency_gemm page, run_kda_projection_overlap:
+ * hidden [M, 7168], packed Q/K/V/G/F_A/beta weight [6288, 7168], F_B weight
+ * [1536, 128], an aux stream running "F_A/beta then F_B", start and
+ * completion events for the fork and the join).
+ *   main:  out_main[M, N_main] = x @ W_main^T                  (h_main)
+ *   aux:   fa[M, N_fa]         = x @ W_fa^T                    (h_fa, bf16 out)
+ *          out_fb[0][M, N_fb]  = fa @ W_fb^T                   (h_fb)
+ *          out_fb[i][M, N_fb]  = out_fb[i-1][:, :K_fb] @ W_fb^T, i = 1..chain-1
+ * out_fb holds `chain` consecutive [M, N_fb] blocks.  h_fb's K must equal
+ * h_fa's N; h_fa must have bf16 output; for chain > 1, h_fb must have bf16
+ * output and N_fb >= K_fb.  Records fork_event on main, makes aux wait on it,
+ * records join_event on aux after the chain and makes main wait on it.  No
+ * synchronization: the whole step can be captured from `main`.
+ */
+int skinny_gemm_run_overlap(skinny_gemm_t h_main, skinny_gemm_t h_fa, skinny_gemm_t h_fb,
+                            int chain, const void* x, int64_t M, void* out_main, void* fa,
+                            void* out_fb, void* main_stream, void* aux_stream,
+                            void* fork_event, void* join_event);
+
+/*
+ * Time the candidate tactics for each M in Ms[0..nM) on this GPU and install
+ * the fastest in the plan; M values not listed take the tuned tactic of the
+ * smallest listed M' >= M that shares their token tile, else keep the default
+ * (low_latency_gemm page, autotune_kda_qkvg: autotune before CUDA graph
+ * capture).  Synchronizes `stream`; allocates and frees a temporary L2-flush
+ * buffer; writes garbage into nothing the caller owns.  Must not be called
+ * while capturing (ECAPTURING).  When SKINNY_GEMM_TACTIC_FILE names a file,
+ * results are appended there and reused by later prepares.
+ */
+int skinny_gemm_autotune(skinny_gemm_t h, const int64_t* Ms, int nM, void* stream);
+
+/* Force the tactic used for token count M (1..64), given as the string
+ * skinny_gemm_plan_query prints.  EINVAL if it does not parse or does not fit
+ * this weight and M. */
+int skinny_gemm_set_tactic(skinny_gemm_t h, int64_t M, const char* tactic);
+
+/* Write the tactic the plan uses for M into buf (NUL-terminated, truncated to
+ * len).  Returns SKG_OK, or EINVAL/EUNSUPPORTED_M. */
+int skinny_gemm_plan_query(skinny_gemm_t h, int64_t M, char* buf, size_t len);
+
+/* Write the candidate tactics valid for this weight at M into buf, separated
+ * by ';'.  Returns the number of candidates (>= 0) or a negated error code. */
+int skinny_gemm_list_tactics(skinny_gemm_t h, int64_t M, char* buf, size_t len);
+
+/* Synchronize `stream`, then read and clear the handle's device status word.
+ * Returns SKG_OK, SKG_ETIMEOUT if a kernel's bounded wait expired since the
+ * last check, or ECUDA.  Not capturable. */
+int skinny_gemm_check_status(skinny_gemm_t h, void* stream);
+
+/* Debug aid for the watchdog: the next `count` launches on this handle
+ * return early after waiting timeout_ns on a barrier that nothing signals,
+ * setting the status word (no output is written).  count 0 clears it. */
+int skinny_gemm_debug_inject_timeout(skinny_gemm_t h, int count, uint64_t timeout_ns);
+
+/* Release the handle (its status word and staging buffers).  The caller must
+ * make sure no launch using it is still pending.  NULL is ignored. */
+void skinny_gemm_destroy(skinny_gemm_t h);
+
+/* Thread-local description of the last failure on this thread ("" if none). */
+const char* skinny_gemm_last_error(void);
+
+/* Thread-local status code of the last failing call on this thread (0 if none);
+ * lets callers of the NULL-returning prepare functions read the reason. */
+int skinny_gemm_last_status(void);
+
+/* SKINNY_GEMM_ABI_VERSION of the loaded library. */
+int skinny_gemm_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SKINNY_GEMM_H_ */

@@ -1,0 +1,801 @@
+// Host side of the C ABI declared in include/skinny_gemm.h: validation,
+// TMA map encoding, the per-M tactic plan, launches (clusters + programmatic
+// dependent launch), the on-device autotuner, the two-stream overlap step and
+// the device watchdog word.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "kernel_params.h"
+#include "skinny_gemm.h"
+
+using namespace skg;
+
+// ------------------------------------------------------------------ errors
+namespace {
+
+thread_local std::string g_err;
+thread_local int g_last_status = 0;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  g_last_status = code;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  if (e == cudaErrorStreamCaptureUnsupported || e == cudaErrorStreamCaptureImplicit ||
+      e == cudaErrorStreamCaptureInvalidated)
+    return fail(SKG_ECAPTURING, "%s: not allowed while a stream is capturing (%s)", what,
+                cudaGetErrorString(e));
+  return fail(SKG_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int ok() {
+  g_err.clear();
+  return SKG_OK;
+}
+
+bool log_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("SKINNY_GEMM_LOG");
+    return v != nullptr && v[0] != '\0' && v[0] != '0';
+  }();
+  return on;
+}
+
+// ------------------------------------------------------------------ driver entry point
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D tile map over a row-major [rows, cols] matrix with row pitch `pitch`
+// elements: box {64, box_rows}, 128-byte swizzle, zero fill outside.
+int encode_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t pitch,
+               int box_rows, int dtype, CUtensorMapL2promotion promo) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return fail(SKG_ECUDA, "cuTensorMapEncodeTiled unavailable from the driver");
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch) * 2u};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBoxK), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType dt =
+      dtype == SKG_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = fn(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, promo,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(SKG_EINVAL, "cuTensorMapEncodeTiled failed (%d) for [%lld, %lld] pitch %lld box %d",
+                static_cast<int>(r), static_cast<long long>(rows), static_cast<long long>(cols),
+                static_cast<long long>(pitch), box_rows);
+  return SKG_OK;
+}
+
+// ------------------------------------------------------------------ kernels / tactics
+struct Tactic {
+  int variant = 0, rows = 0, tok = 0, nbox = 0, stages = 0, cl = 0;
+  bool valid() const { return variant != 0; }
+};
+
+std::string tactic_str(const Tactic& t) {
+  char b[96];
+  snprintf(b, sizeof b, "%s:r%d:t%d:b%d:s%d:c%d", t.variant == kVariantTc ? "tc" : "mma", t.rows,
+           t.tok, t.nbox, t.stages, t.cl);
+  return b;
+}
+
+bool tactic_parse(const char* s, Tactic* t) {
+  char kind[16] = {0};
+  Tactic x;
+  if (s == nullptr ||
+      sscanf(s, "%15[^:]:r%d:t%d:b%d:s%d:c%d", kind, &x.rows, &x.tok, &x.nbox, &x.stages, &x.cl) != 6)
+    return false;
+  if (strcmp(kind, "tc") == 0)
+    x.variant = kVariantTc;
+  else if (strcmp(kind, "mma") == 0)
+    x.variant = kVariantMma;
+  else
+    return false;
+  *t = x;
+  return true;
+}
+
+const KernelEntry* find_kernel(const Tactic& t, int in_dtype, int out_dtype) {
+  int n = 0;
+  const KernelEntry* tab = t.variant == kVariantTc ? tc_kernel_table(&n) : mma_kernel_table(&n);
+  for (int i = 0; i < n; ++i)
+    if (tab[i].rows == t.rows && tab[i].tok == t.tok && tab[i].nbox == t.nbox &&
+        tab[i].in_dtype == in_dtype && tab[i].out_dtype == out_dtype)
+      return &tab[i];
+  return nullptr;
+}
+
+std::vector<const KernelEntry*> all_kernels() {
+  std::vector<const KernelEntry*> v;
+  int n = 0;
+  const KernelEntry* a = tc_kernel_table(&n);
+  for (int i = 0; i < n; ++i) v.push_back(&a[i]);
+  a = mma_kernel_table(&n);
+  for (int i = 0; i < n; ++i) v.push_back(&a[i]);
+  return v;
+}
+
+struct DeviceInfo {
+  int sm_count = 0, smem_optin = 0, l2_bytes = 0, major = 0, minor = 0;
+  char name[256] = {0};
+  bool attrs_set = false;
+};
+
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+
+int device_info(int dev, DeviceInfo** out) {
+  if (dev < 0 || dev >= 64) return fail(SKG_EDEVICE, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.attrs_set) {
+    cudaDeviceProp prop;
+    cudaError_t e = cudaGetDeviceProperties(&prop, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+    d.sm_count = prop.multiProcessorCount;
+    d.smem_optin = static_cast<int>(prop.sharedMemPerBlockOptin);
+    d.l2_bytes = prop.l2CacheSize;
+    d.major = prop.major;
+    d.minor = prop.minor;
+    snprintf(d.name, sizeof d.name, "%s", prop.name);
+    if (!(d.major == 10 && d.minor == 3))
+      return fail(SKG_EDEVICE, "device %d is sm_%d%d; this library is built for sm_103a only", dev,
+                  d.major, d.minor);
+    for (const KernelEntry* k : all_kernels()) {
+      e = cudaFuncSetAttribute(k->func, cudaFuncAttributeMaxDynamicSharedMemorySize, d.smem_optin);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic smem)");
+      e = cudaFuncSetAttribute(k->func, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(non-portable cluster)");
+    }
+    d.attrs_set = true;
+  }
+  *out = &d;
+  return SKG_OK;
+}
+
+uint64_t env_u64(const char* name, uint64_t dflt) {
+  const char* v = getenv(name);
+  if (v == nullptr || *v == '\0') return dflt;
+  return strtoull(v, nullptr, 10);
+}
+
+const int kTcToks[] = {16, 32, 64};
+const int kMmaToks[] = {8, 16, 32};
+const int kClusters[] = {1, 2, 4, 8, 16};
+
+}  // namespace
+
+// ------------------------------------------------------------------ handle
+struct skinny_gemm_plan {
+  const void* W = nullptr;
+  int64_t N = 0, K = 0, ldw = 0;
+  int dtype = SKG_BF16, out_dtype = SKG_BF16;
+  int device = 0;
+  DeviceInfo* dev = nullptr;
+  int kboxes = 0;
+  CUtensorMap wmap64{}, wmap128{};
+  Tactic plan[SKINNY_GEMM_MAX_M + 1];
+  uint32_t* status = nullptr;
+  void* x_stage = nullptr;
+  void* out_stage = nullptr;
+  uint64_t timeout_ns = 2000000000ull;
+  int debug_count = 0;
+  uint64_t debug_timeout_ns = 0;
+};
+
+namespace {
+
+int out_elem_bytes(const skinny_gemm_plan* h) { return h->out_dtype == SKG_FP32 ? 4 : 2; }
+
+// Validity of tactic t for this weight at token count M (M = 0: any M <= tok).
+bool tactic_fits(const skinny_gemm_plan* h, const Tactic& t, int64_t M, std::string* why) {
+  auto no = [&](const char* w) {
+    if (why) *why = w;
+    return false;
+  };
+  if (!t.valid()) return no("empty tactic");
+  const KernelEntry* k = find_kernel(t, h->dtype, h->out_dtype);
+  if (k == nullptr) return no("no compiled kernel for this rows/tok/box/dtype combination");
+  if (M > t.tok) return no("token tile smaller than M");
+  bool pow2 = false;
+  for (int c : kClusters) pow2 |= (c == t.cl);
+  if (!pow2) return no("cluster size must be 1, 2, 4, 8 or 16");
+  if (t.cl > h->kboxes) return no("cluster larger than the number of 64-wide K blocks");
+  if (t.rows % t.cl != 0) return no("cluster size must divide the row tile");
+  if (t.stages < 1 || t.stages > 16) return no("stages out of range 1..16");
+  if (static_cast<int>(smem_bytes(t.rows, t.tok, t.nbox, t.stages)) > h->dev->smem_optin)
+    return no("shared memory footprint exceeds the per-block limit");
+  return true;
+}
+
+int launch_tactic(skinny_gemm_plan* h, const Tactic& t, const void* x, int64_t ldx, int64_t M,
+                  void* out, int64_t ldo, cudaStream_t st) {
+  const KernelEntry* k = find_kernel(t, h->dtype, h->out_dtype);
+  if (k == nullptr) return fail(SKG_EINVAL, "no kernel for tactic %s", tactic_str(t).c_str());
+  CUtensorMap xmap;
+  int rc = encode_map(&xmap, x, M, h->K, ldx, t.tok, h->dtype, CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
+  if (rc != SKG_OK) return rc;
+  KParams p{};
+  p.out = out;
+  p.ldo = ldo;
+  p.M = static_cast<int32_t>(M);
+  p.N = static_cast<int32_t>(h->N);
+  p.kboxes = h->kboxes;
+  p.stages = t.stages;
+  p.status = h->status;
+  p.timeout_ns = h->timeout_ns;
+  if (h->debug_count > 0) {
+    --h->debug_count;
+    p.debug_wait = 1;
+    p.timeout_ns = h->debug_timeout_ns;
+  }
+  const int ntiles = static_cast<int>((h->N + t.rows - 1) / t.rows);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(ntiles * t.cl), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(k->threads), 1, 1);
+  cfg.dynamicSmemBytes = smem_bytes(t.rows, t.tok, t.nbox, t.stages);
+  cfg.stream = st;
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = static_cast<unsigned>(t.cl);
+  attrs[0].val.clusterDim.y = 1;
+  attrs[0].val.clusterDim.z = 1;
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 2;
+  const CUtensorMap* wmap = t.rows == 64 ? &h->wmap64 : &h->wmap128;
+  void* args[3] = {const_cast<CUtensorMap*>(wmap), &xmap, &p};
+  cudaError_t e = cudaLaunchKernelExC(&cfg, k->func, args);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelExC");
+  return SKG_OK;
+}
+
+// Clusters of this tactic that fit on the GPU at once (0: cannot launch).
+int active_clusters(const skinny_gemm_plan* h, const Tactic& t) {
+  const KernelEntry* k = find_kernel(t, h->dtype, h->out_dtype);
+  if (k == nullptr) return 0;
+  cudaLaunchConfig_t cfg{};
+  const int ntiles = static_cast<int>((h->N + t.rows - 1) / t.rows);
+  cfg.gridDim = dim3(static_cast<unsigned>(ntiles * t.cl), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(k->threads), 1, 1);
+  cfg.dynamicSmemBytes = smem_bytes(t.rows, t.tok, t.nbox, t.stages);
+  cudaLaunchAttribute a[1];
+  a[0].id = cudaLaunchAttributeClusterDimension;
+  a[0].val.clusterDim.x = static_cast<unsigned>(t.cl);
+  a[0].val.clusterDim.y = 1;
+  a[0].val.clusterDim.z = 1;
+  cfg.attrs = a;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k->func, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+// Candidate tactics for M: the smallest token tile >= M of each variant,
+// every stage count / box count / cluster size that fits and can launch.
+std::vector<Tactic> candidates(const skinny_gemm_plan* h, int64_t M) {
+  std::vector<Tactic> out;
+  for (int variant : {kVariantTc, kVariantMma}) {
+    const int* toks = variant == kVariantTc ? kTcToks : kMmaToks;
+    int tok = 0;
+    for (int i = 0; i < 3; ++i)
+      if (toks[i] >= M) {
+        tok = toks[i];
+        break;
+      }
+    if (tok == 0) continue;
+    for (const KernelEntry* k : all_kernels()) {
+      if (k->variant != variant || k->tok != tok || k->in_dtype != h->dtype ||
+          k->out_dtype != h->out_dtype)
+        continue;
+      for (int cl : kClusters)
+        for (int s = 2; s <= 8; ++s) {
+          Tactic t{variant, k->rows, tok, k->nbox, s, cl};
+          if (!tactic_fits(h, t, M, nullptr)) continue;
+          if (active_clusters(h, t) <= 0) continue;
+          out.push_back(t);
+        }
+    }
+  }
+  return out;
+}
+
+// Default (untuned) choice: tcgen05 kernel, the smallest token tile >= M,
+// two 64-wide boxes per stage, the cluster split that first gives at least
+// one CTA per SM, and as many stages as fit two CTAs per SM (one when the
+// grid is smaller than the GPU).
+Tactic default_tactic(const skinny_gemm_plan* h, int64_t M) {
+  Tactic best;
+  int tok = 0;
+  for (int tk : kTcToks)
+    if (tk >= M) {
+      tok = tk;
+      break;
+    }
+  if (tok == 0) return best;
+  const int rows = 128;
+  const int ntiles = static_cast<int>((h->N + rows - 1) / rows);
+  int cl = 1;
+  while (cl < 8 && ntiles * cl < h->dev->sm_count && cl * 2 <= h->kboxes) cl *= 2;
+  const int ctas = ntiles * cl;
+  const int per_sm = ctas > h->dev->sm_count ? 2 : 1;
+  const int budget = h->dev->smem_optin / per_sm - 2048;
+  const int nbox = 2;
+  const int per_cta_boxes = (h->kboxes + cl - 1) / cl;
+  const int max_iters = (per_cta_boxes + nbox - 1) / nbox;
+  int stages = 2;
+  while (stages < 8 && stages < max_iters &&
+         static_cast<int>(smem_bytes(rows, tok, nbox, stages + 1)) <= budget)
+    ++stages;
+  Tactic t{kVariantTc, rows, tok, nbox, stages, cl};
+  if (tactic_fits(h, t, M, nullptr)) return t;
+  for (int s = stages; s >= 1; --s) {
+    t.stages = s;
+    if (tactic_fits(h, t, M, nullptr)) return t;
+  }
+  return best;
+}
+
+// ------------------------------------------------------------------ tactic file
+const char* out_name(int d) { return d == SKG_FP32 ? "fp32" : (d == SKG_FP16 ? "fp16" : "bf16"); }
+
+std::string cache_key(const skinny_gemm_plan* h) {
+  char b[512];
+  snprintf(b, sizeof b, "%s|sm%d|N%lld|K%lld|in%s|out%s|abi%d", h->dev->name, h->dev->sm_count,
+           static_cast<long long>(h->N), static_cast<long long>(h->K), out_name(h->dtype),
+           out_name(h->out_dtype), SKINNY_GEMM_ABI_VERSION);
+  return b;
+}
+
+void load_tactic_file(skinny_gemm_plan* h) {
+  const char* path = getenv("SKINNY_GEMM_TACTIC_FILE");
+  if (path == nullptr || *path == '\0') return;
+  FILE* f = fopen(path, "r");
+  if (f == nullptr) return;
+  const std::string key = cache_key(h);
+  char line[1024];
+  while (fgets(line, sizeof line, f) != nullptr) {
+    // line: <key> <M> <tactic> <us>
+    char k[600], ts[96];
+    int m = 0;
+    double us = 0;
+    if (sscanf(line, "%599s %d %95s %lf", k, &m, ts, &us) < 3) continue;
+    Tactic t;
+    if (key != k || m < 1 || m > SKINNY_GEMM_MAX_M || !tactic_parse(ts, &t)) continue;
+    if (tactic_fits(h, t, m, nullptr) && active_clusters(h, t) > 0) h->plan[m] = t;  // last wins
+  }
+  fclose(f);
+}
+
+void append_tactic_file(const skinny_gemm_plan* h, int64_t M, const Tactic& t, double us) {
+  const char* path = getenv("SKINNY_GEMM_TACTIC_FILE");
+  if (path == nullptr || *path == '\0') return;
+  FILE* f = fopen(path, "a");
+  if (f == nullptr) return;
+  fprintf(f, "%s %lld %s %.3f\n", cache_key(h).c_str(), static_cast<long long>(M),
+          tactic_str(t).c_str(), us);
+  fclose(f);
+}
+
+// ------------------------------------------------------------------ L2 flush (autotuner)
+__global__ void l2_flush_kernel(const uint4* __restrict__ buf, size_t n, uint32_t* sink) {
+  uint32_t acc = 0;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const uint4 v = __ldcs(buf + i);
+    acc ^= v.x ^ v.y ^ v.z ^ v.w;
+  }
+  if (acc == 0x9E3779B9u && sink != nullptr) *sink = acc;  // keeps the loads alive
+}
+
+int check_handle(const skinny_gemm_plan* h) {
+  if (h == nullptr) return fail(SKG_EINVAL, "null handle");
+  return SKG_OK;
+}
+
+int validate_run(const skinny_gemm_plan* h, const void* x, int64_t ldx, int64_t M, const void* out,
+                 int64_t ldo) {
+  if (check_handle(h) != SKG_OK) return SKG_EINVAL;
+  if (M < 1 || M > SKINNY_GEMM_MAX_M)
+    return fail(SKG_EUNSUPPORTED_M, "M = %lld outside 1..%d: fall back", static_cast<long long>(M),
+                SKINNY_GEMM_MAX_M);
+  if (x == nullptr || out == nullptr) return fail(SKG_EINVAL, "null x or out");
+  if (ldx < h->K || ldo < h->N)
+    return fail(SKG_EINVAL, "row pitch too small: ldx %lld (K %lld), ldo %lld (N %lld)",
+                static_cast<long long>(ldx), static_cast<long long>(h->K),
+                static_cast<long long>(ldo), static_cast<long long>(h->N));
+  if (reinterpret_cast<uintptr_t>(x) % 16 || reinterpret_cast<uintptr_t>(out) % 16)
+    return fail(SKG_EALIGN, "x and out must be 16-byte aligned");
+  if ((ldx * 2) % 16) return fail(SKG_EALIGN, "x row pitch must be a multiple of 16 bytes");
+  return SKG_OK;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ C ABI
+extern "C" {
+
+int skinny_gemm_abi_version(void) { return SKINNY_GEMM_ABI_VERSION; }
+
+const char* skinny_gemm_last_error(void) { return g_err.c_str(); }
+
+int skinny_gemm_last_status(void) { return g_last_status; }
+
+skinny_gemm_t skinny_gemm_prepare_ex(const void* W, int64_t N, int64_t K, int64_t ldw, int dtype,
+                                     int out_dtype, unsigned flags) {
+  g_last_status = 0;
+  if (W == nullptr) return fail(SKG_EINVAL, "null weight pointer"), nullptr;
+  if (dtype != SKG_BF16)
+    return fail(SKG_EINVAL, "weight dtype %d unsupported: BF16 only", dtype), nullptr;
+  if (out_dtype != SKG_BF16 && out_dtype != SKG_FP32)
+    return fail(SKG_EINVAL, "unsupported projection output dtype %d (BF16 or FP32)", out_dtype),
+           nullptr;
+  if (N < 1 || K < 8 || N > (1ll << 31) - 1 || K > (1ll << 31) - 1)
+    return fail(SKG_EINVAL, "weight shape [%lld, %lld] out of range", static_cast<long long>(N),
+                static_cast<long long>(K)),
+           nullptr;
+  if (K % 8 != 0)
+    return fail(SKG_EALIGN, "K = %lld: rows need a 16-byte multiple length (K %% 8 == 0)",
+                static_cast<long long>(K)),
+           nullptr;
+  if (ldw < K || ldw % 8 != 0)
+    return fail(SKG_EALIGN, "weight rows need unit stride and a 16 B TMA pitch (ldw %lld)",
+                static_cast<long long>(ldw)),
+           nullptr;
+  if (reinterpret_cast<uintptr_t>(W) % 16 != 0)
+    return fail(SKG_EALIGN, "weight base must be 16-byte aligned"), nullptr;
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice"), nullptr;
+  DeviceInfo* di = nullptr;
+  if (device_info(dev, &di) != SKG_OK) return nullptr;
+
+  auto* h = new skinny_gemm_plan();
+  h->W = W;
+  h->N = N;
+  h->K = K;
+  h->ldw = ldw;
+  h->dtype = dtype;
+  h->out_dtype = out_dtype;
+  h->device = dev;
+  h->dev = di;
+  h->kboxes = static_cast<int>((K + kBoxK - 1) / kBoxK);
+  h->timeout_ns = env_u64("SKINNY_GEMM_TIMEOUT_NS", 2000000000ull);
+  if (encode_map(&h->wmap64, W, N, K, ldw, 64, dtype, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) != SKG_OK ||
+      encode_map(&h->wmap128, W, N, K, ldw, 128, dtype, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) != SKG_OK) {
+    delete h;
+    return nullptr;
+  }
+  e = cudaMalloc(&h->status, sizeof(uint32_t));
+  if (e != cudaSuccess) {
+    h->status = nullptr;
+    cuda_fail(e, "cudaMalloc(status word)");
+    delete h;
+    return nullptr;
+  }
+  e = cudaMemset(h->status, 0, sizeof(uint32_t));
+  if (e != cudaSuccess) {
+    cuda_fail(e, "cudaMemset(status word)");
+    skinny_gemm_destroy(h);
+    return nullptr;
+  }
+  for (int m = 1; m <= SKINNY_GEMM_MAX_M; ++m) h->plan[m] = default_tactic(h, m);
+  if (!(flags & SKG_PREPARE_NO_TUNE_CACHE)) load_tactic_file(h);
+  if (const char* f = getenv("SKINNY_GEMM_FORCE_TACTIC")) {
+    Tactic t;
+    if (tactic_parse(f, &t))
+      for (int m = 1; m <= SKINNY_GEMM_MAX_M; ++m)
+        if (tactic_fits(h, t, m, nullptr)) h->plan[m] = t;
+  }
+  for (int m = 1; m <= SKINNY_GEMM_MAX_M; ++m)
+    if (!h->plan[m].valid()) {
+      fail(SKG_EINVAL, "no valid tactic for M = %d on this weight", m);
+      skinny_gemm_destroy(h);
+      return nullptr;
+    }
+  if (log_enabled()) {
+    fprintf(stderr, "[skinny_gemm] prepared N=%lld K=%lld on %s (%d SMs):", static_cast<long long>(N),
+            static_cast<long long>(K), di->name, di->sm_count);
+    for (int m : {1, 2, 4, 8, 16, 32, 48, 64}) fprintf(stderr, " M%d=%s", m, tactic_str(h->plan[m]).c_str());
+    fprintf(stderr, "\n");
+  }
+  ok();
+  return h;
+}
+
+skinny_gemm_t skinny_gemm_prepare(const void* W, int64_t N, int64_t K, int dtype, int out_dtype) {
+  return skinny_gemm_prepare_ex(W, N, K, K, dtype, out_dtype, 0u);
+}
+
+int skinny_gemm_run_strided(skinny_gemm_t h, const void* x, int64_t ldx, int64_t M, void* out,
+                            int64_t ldo, void* stream) {
+  int rc = validate_run(h, x, ldx, M, out, ldo);
+  if (rc != SKG_OK) return rc;
+  rc = launch_tactic(h, h->plan[M], x, ldx, M, out, ldo, static_cast<cudaStream_t>(stream));
+  return rc == SKG_OK ? ok() : rc;
+}
+
+int skinny_gemm_run(skinny_gemm_t h, const void* x, int64_t M, void* out, void* stream) {
+  if (check_handle(h) != SKG_OK) return SKG_EINVAL;
+  return skinny_gemm_run_strided(h, x, h->K, M, out, h->N, stream);
+}
+
+int skinny_gemm_run_host(skinny_gemm_t h, const void* x_host, int64_t M, void* out_host,
+                         void* stream) {
+  if (check_handle(h) != SKG_OK) return SKG_EINVAL;
+  if (x_host == nullptr || out_host == nullptr) return fail(SKG_EINVAL, "null host buffer");
+  if (M < 1 || M > SKINNY_GEMM_MAX_M)
+    return fail(SKG_EUNSUPPORTED_M, "M = %lld outside 1..%d", static_cast<long long>(M),
+                SKINNY_GEMM_MAX_M);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (h->x_stage == nullptr) {
+    e = cudaMalloc(&h->x_stage, static_cast<size_t>(SKINNY_GEMM_MAX_M) * h->K * 2);
+    if (e != cudaSuccess) return h->x_stage = nullptr, cuda_fail(e, "cudaMalloc(x staging)");
+  }
+  if (h->out_stage == nullptr) {
+    e = cudaMalloc(&h->out_stage, static_cast<size_t>(SKINNY_GEMM_MAX_M) * h->N * out_elem_bytes(h));
+    if (e != cudaSuccess) return h->out_stage = nullptr, cuda_fail(e, "cudaMalloc(out staging)");
+  }
+  e = cudaMemcpyAsync(h->x_stage, x_host, static_cast<size_t>(M) * h->K * 2, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(x)");
+  int rc = skinny_gemm_run(h, h->x_stage, M, h->out_stage, stream);
+  if (rc != SKG_OK) return rc;
+  e = cudaMemcpyAsync(out_host, h->out_stage, static_cast<size_t>(M) * h->N * out_elem_bytes(h),
+                      cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(out)");
+  e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  return ok();
+}
+
+int skinny_gemm_run_overlap(skinny_gemm_t h_main, skinny_gemm_t h_fa, skinny_gemm_t h_fb, int chain,
+                            const void* x, int64_t M, void* out_main, void* fa, void* out_fb,
+                            void* main_stream, void* aux_stream, void* fork_event,
+                            void* join_event) {
+  if (h_main == nullptr || h_fa == nullptr || h_fb == nullptr)
+    return fail(SKG_EINVAL, "null handle");
+  if (chain < 1) return fail(SKG_EINVAL, "chain must be >= 1");
+  if (h_fa->K != h_main->K) return fail(SKG_EINVAL, "F_A and main weights need the same K");
+  if (h_fa->out_dtype != SKG_BF16) return fail(SKG_EINVAL, "F_A output must be bf16 (it feeds F_B)");
+  if (h_fb->K != h_fa->N) return fail(SKG_EINVAL, "F_B K must equal F_A N");
+  if (chain > 1 && (h_fb->out_dtype != SKG_BF16 || h_fb->N < h_fb->K))
+    return fail(SKG_EINVAL, "a chain needs bf16 F_B output with N_fb >= K_fb");
+  if (fork_event == nullptr || join_event == nullptr || aux_stream == nullptr)
+    return fail(SKG_EINVAL, "overlap needs an aux stream and two events");
+  int rc = validate_run(h_main, x, h_main->K, M, out_main, h_main->N);
+  if (rc != SKG_OK) return rc;
+  rc = validate_run(h_fa, x, h_fa->K, M, fa, h_fa->N);
+  if (rc != SKG_OK) return rc;
+  cudaStream_t ms = static_cast<cudaStream_t>(main_stream);
+  cudaStream_t as = static_cast<cudaStream_t>(aux_stream);
+  cudaEvent_t fork = static_cast<cudaEvent_t>(fork_event);
+  cudaEvent_t join = static_cast<cudaEvent_t>(join_event);
+  cudaError_t e = cudaEventRecord(fork, ms);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(fork)");
+  e = cudaStreamWaitEvent(as, fork, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent(aux, fork)");
+  // Aux chain first so its small grids are queued before the big one fills the GPU.
+  rc = launch_tactic(h_fa, h_fa->plan[M], x, h_fa->K, M, fa, h_fa->N, as);
+  if (rc != SKG_OK) return rc;
+  const size_t blk = static_cast<size_t>(M) * h_fb->N * out_elem_bytes(h_fb);
+  char* fb = static_cast<char*>(out_fb);
+  rc = launch_tactic(h_fb, h_fb->plan[M], fa, h_fb->K, M, fb, h_fb->N, as);
+  if (rc != SKG_OK) return rc;
+  for (int i = 1; i < chain; ++i) {
+    rc = launch_tactic(h_fb, h_fb->plan[M], fb + (i - 1) * blk, h_fb->N, M, fb + i * blk, h_fb->N, as);
+    if (rc != SKG_OK) return rc;
+  }
+  e = cudaEventRecord(join, as);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(join)");
+  rc = launch_tactic(h_main, h_main->plan[M], x, h_main->K, M, out_main, h_main->N, ms);
+  if (rc != SKG_OK) return rc;
+  e = cudaStreamWaitEvent(ms, join, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent(main, join)");
+  return ok();
+}
+
+int skinny_gemm_set_tactic(skinny_gemm_t h, int64_t M, const char* tactic) {
+  if (check_handle(h) != SKG_OK) return SKG_EINVAL;
+  if (M < 1 || M > SKINNY_GEMM_MAX_M)
+    return fail(SKG_EUNSUPPORTED_M, "M = %lld outside 1..%d", static_cast<long long>(M),
+                SKINNY_GEMM_MAX_M);
+  Tactic t;
+  if (!tactic_parse(tactic, &t)) return fail(SKG_EINVAL, "cannot parse tactic '%s'", tactic ? tactic : "");
+  std::string why;
+  if (!tactic_fits(h, t, M, &why))
+    return fail(SKG_EINVAL, "tactic %s does not fit: %s", tactic, why.c_str());
+  if (active_clusters(h, t) <= 0)
+    return fail(SKG_EINVAL, "tactic %s cannot be resident on this GPU", tactic);
+  h->plan[M] = t;
+  return ok();
+}
+
+int skinny_gemm_plan_query(skinny_gemm_t h, int64_t M, char* buf, size_t len) {
+  if (check_handle(h) != SKG_OK) return SKG_EINVAL;
+  if (M < 1 || M > SKINNY_GEMM_MAX_M)
+    return fail(SKG_EUNSUPPORTED_M, "M = %lld outside 1..%d", static_cast<long long>(M),
+                SKINNY_GEMM_MAX_M);
+  if (buf == nullptr || len == 0) return fail(SKG_EINVAL, "null buffer");
+  snprintf(buf, len, "%s", tactic_str(h->plan[M]).c_str());
+  return ok();
+}
+
+int skinny_gemm_list_tactics(skinny_gemm_t h, int64_t M, char* buf, size_t len) {
+  if (check_handle(h) != SKG_OK) return -SKG_EINVAL;
+  if (M < 1 || M > SKINNY_GEMM_MAX_M) return -fail(SKG_EUNSUPPORTED_M, "M out of range");
+  std::vector<Tactic> c = candidates(h, M);
+  std::string s;
+  for (size_t i = 0; i < c.size(); ++i) {
+    if (i) s += ';';
+    s += tactic_str(c[i]);
+  }
+  if (buf != nullptr && len > 0) snprintf(buf, len, "%s", s.c_str());
+  ok();
+  return static_cast<int>(c.size());
+}
+
+int skinny_gemm_autotune(skinny_gemm_t h, const int64_t* Ms, int nM, void* stream) {
+  if (check_handle(h) != SKG_OK) return SKG_EINVAL;
+  if (Ms == nullptr || nM < 1) return fail(SKG_EINVAL, "no token counts to tune");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(st, &cs);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+  if (cs != cudaStreamCaptureStatusNone)
+    return fail(SKG_ECAPTURING, "autotune must run before CUDA graph capture");
+  for (int i = 0; i < nM; ++i)
+    if (Ms[i] < 1 || Ms[i] > SKINNY_GEMM_MAX_M)
+      return fail(SKG_EUNSUPPORTED_M, "M = %lld outside 1..%d", static_cast<long long>(Ms[i]),
+                  SKINNY_GEMM_MAX_M);
+  const int reps = static_cast<int>(env_u64("SKINNY_GEMM_TUNE_REPS", 9));
+  const size_t flush_bytes = static_cast<size_t>(std::max(h->dev->l2_bytes, 1 << 20)) * 2;
+  void *flush = nullptr, *xbuf = nullptr, *obuf = nullptr;
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  int rc = SKG_OK;
+  std::vector<float> times;
+  auto cleanup = [&]() {
+    if (flush) cudaFree(flush);
+    if (xbuf) cudaFree(xbuf);
+    if (obuf) cudaFree(obuf);
+    if (e0) cudaEventDestroy(e0);
+    if (e1) cudaEventDestroy(e1);
+  };
+  if ((e = cudaMalloc(&flush, flush_bytes)) != cudaSuccess ||
+      (e = cudaMalloc(&xbuf, static_cast<size_t>(SKINNY_GEMM_MAX_M) * h->K * 2)) != cudaSuccess ||
+      (e = cudaMalloc(&obuf, static_cast<size_t>(SKINNY_GEMM_MAX_M) * h->N * 4)) != cudaSuccess ||
+      (e = cudaMemsetAsync(flush, 0, flush_bytes, st)) != cudaSuccess ||
+      (e = cudaMemsetAsync(xbuf, 0, static_cast<size_t>(SKINNY_GEMM_MAX_M) * h->K * 2, st)) != cudaSuccess ||
+      (e = cudaEventCreate(&e0)) != cudaSuccess || (e = cudaEventCreate(&e1)) != cudaSuccess) {
+    cleanup();
+    return cuda_fail(e, "autotune setup");
+  }
+  std::vector<int64_t> tuned;
+  for (int i = 0; i < nM && rc == SKG_OK; ++i) {
+    const int64_t M = Ms[i];
+    std::vector<Tactic> cand = candidates(h, M);
+    double best_us = 1e30;
+    Tactic best;
+    for (const Tactic& t : cand) {
+      times.clear();
+      rc = launch_tactic(h, t, xbuf, h->K, M, obuf, h->N, st);  // warm-up
+      for (int r = 0; r < reps && rc == SKG_OK; ++r) {
+        l2_flush_kernel<<<h->dev->sm_count * 4, 512, 0, st>>>(static_cast<const uint4*>(flush),
+                                                             flush_bytes / 16, nullptr);
+        cudaEventRecord(e0, st);
+        rc = launch_tactic(h, t, xbuf, h->K, M, obuf, h->N, st);
+        cudaEventRecord(e1, st);
+        if (rc != SKG_OK) break;
+        if ((e = cudaEventSynchronize(e1)) != cudaSuccess) {
+          rc = cuda_fail(e, "autotune timing");
+          break;
+        }
+        float ms = 0;
+        cudaEventElapsedTime(&ms, e0, e1);
+        times.push_back(ms);
+      }
+      if (rc != SKG_OK) break;
+      std::sort(times.begin(), times.end());
+      const double us = 1000.0 * times[times.size() / 2];
+      if (log_enabled())
+        fprintf(stderr, "[skinny_gemm] tune N=%lld K=%lld M=%lld %s %.2f us\n",
+                static_cast<long long>(h->N), static_cast<long long>(h->K),
+                static_cast<long long>(M), tactic_str(t).c_str(), us);
+      if (us < best_us) {
+        best_us = us;
+        best = t;
+      }
+    }
+    if (rc == SKG_OK && best.valid()) {
+      h->plan[M] = best;
+      tuned.push_back(M);
+      append_tactic_file(h, M, best, best_us);
+    }
+  }
+  e = cudaStreamSynchronize(st);
+  cleanup();
+  if (rc != SKG_OK) return rc;
+  if (e != cudaSuccess) return cuda_fail(e, "autotune sync");
+  // Untuned M take the tuned tactic of the smallest tuned M' >= M.
+  std::sort(tuned.begin(), tuned.end());
+  for (int m = 1; m <= SKINNY_GEMM_MAX_M; ++m) {
+    if (std::binary_search(tuned.begin(), tuned.end(), static_cast<int64_t>(m))) continue;
+    for (int64_t mp : tuned)
+      if (mp >= m) {
+        if (tactic_fits(h, h->plan[mp], m, nullptr)) h->plan[m] = h->plan[mp];
+        break;
+      }
+  }
+  return ok();
+}
+
+int skinny_gemm_check_status(skinny_gemm_t h, void* stream) {
+  if (check_handle(h) != SKG_OK) return SKG_EINVAL;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  uint32_t v = 0;
+  e = cudaMemcpy(&v, h->status, sizeof v, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(status)");
+  if (v != 0) {
+    cudaMemset(h->status, 0, sizeof v);
+    return fail(SKG_ETIMEOUT, "device watchdog: bounded wait expired (code 0x%08x)", v);
+  }
+  return ok();
+}
+
+int skinny_gemm_debug_inject_timeout(skinny_gemm_t h, int count, uint64_t timeout_ns) {
+  if (check_handle(h) != SKG_OK) return SKG_EINVAL;
+  if (count < 0) return fail(SKG_EINVAL, "negative count");
+  h->debug_count = count;
+  h->debug_timeout_ns = timeout_ns;
+  return ok();
+}
+
+void skinny_gemm_destroy(skinny_gemm_t h) {
+  if (h == nullptr) return;
+  if (h->status) cudaFree(h->status);
+  if (h->x_stage) cudaFree(h->x_stage);
+  if (h->out_stage) cudaFree(h->out_stage);
+  delete h;
+}
+
+}  // extern "C"

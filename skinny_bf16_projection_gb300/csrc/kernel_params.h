@@ -1,0 +1,66 @@
+// Launch parameters and the kernel registry shared by the host library and
+// the kernel translation units.
+#pragma once
+
+#include <cstdint>
+
+namespace skg {
+
+constexpr int kBoxK = 64;            // bf16 elements per TMA box row (128 bytes)
+constexpr int kBoxRowBytes = 128;
+constexpr int kSmemAlign = 1024;     // 128-byte swizzle atoms are 8 rows x 128 B
+
+// Status codes written into the device status word (first error wins).
+enum : uint32_t {
+  kStatusTimeoutFull = 0x10000001u,   // waiting for a stage's TMA data
+  kStatusTimeoutEmpty = 0x10000002u,  // producer waiting for a stage to drain
+  kStatusTimeoutDone = 0x10000003u,   // waiting for the MMAs to finish
+  kStatusTimeoutRecv = 0x10000004u,   // waiting for cluster peers' partial sums
+  kStatusTimeoutDebug = 0x10000005u,  // injected watchdog self-test
+  kStatusTimeoutDrain = 0x10000006u,  // final drain of in-flight copies
+};
+
+struct KParams {
+  void* out;              // [M, ldo] row-major, output element type of the kernel
+  int64_t ldo;            // output row pitch (elements)
+  int32_t M;              // valid tokens, 1..TOK
+  int32_t N;              // valid weight rows
+  int32_t kboxes;         // ceil(K / 64): 64-wide K blocks of the weight
+  int32_t stages;         // pipeline depth (shared-memory stages)
+  uint32_t* status;       // device status word (watchdog)
+  uint64_t timeout_ns;    // bound of every spin wait
+  int32_t debug_wait;     // nonzero: watchdog self-test, wait on a dead barrier and return
+  int32_t pad_;
+};
+
+// Shared-memory footprint of one configuration (bytes, including 1 KB of
+// alignment slack).  Same formula on host and device.
+__host__ __device__ constexpr uint32_t stage_bytes(int rows, int tok, int nbox) {
+  return static_cast<uint32_t>(nbox * (rows + tok) * kBoxRowBytes);
+}
+__host__ __device__ constexpr uint32_t red_bytes(int rows, int tok) {
+  return static_cast<uint32_t>(rows * tok * 4);
+}
+__host__ __device__ constexpr uint32_t smem_bytes(int rows, int tok, int nbox, int stages) {
+  return kSmemAlign + stages * stage_bytes(rows, tok, nbox) + red_bytes(rows, tok) +
+         static_cast<uint32_t>((2 * stages + 4) * 8) + 16;
+}
+
+enum Variant : int { kVariantMma = 1, kVariantTc = 2 };
+
+struct KernelEntry {
+  int variant;    // kVariantMma (mma.sync) or kVariantTc (tcgen05 / TMEM)
+  int rows;       // weight rows per CTA tile
+  int tok;        // token tile (MMA N)
+  int nbox;       // 64-wide K boxes per pipeline stage
+  int in_dtype;   // 0 bf16, 1 fp16 (skinny_gemm_dtype)
+  int out_dtype;  // 0 bf16, 2 fp32
+  int threads;    // CTA size
+  const void* func;
+};
+
+// Defined in kernels_mma.cu and kernels_tc.cu.
+const KernelEntry* mma_kernel_table(int* count);
+const KernelEntry* tc_kernel_table(int* count);
+
+}  // namespace skg

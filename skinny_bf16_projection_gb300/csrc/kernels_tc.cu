@@ -1,0 +1,259 @@
+// Split-K skinny projection on the 5th-generation tensor cores (tcgen05/TMEM).
+//
+//   out[M, N] = x[M, K] @ W[N, K]^T,  M <= 64, computed swap-AB: the MMA's M
+//   dimension is 128 weight rows, its N dimension the token tile, so the
+//   accumulator D[128 rows][TOK tokens] (fp32) lives in TMEM and the weight
+//   tile is the MMA's A operand straight from TMA-written shared memory.
+//
+// Design points taken from the pages (page "vllm.models.glm5next.nvidia.
+// specialized_decode.gemm", module docstring: split-K tcgen05 GEMM with a
+// cluster DSMEM reduction and an evict-first weight TMA; page "vllm.models.
+// kimi_k3.nvidia.specialized_decode.cutedsl.gemm.projection", weight_map: a
+// TMA map of W with box {64, rows} and 128-byte swizzle; output view
+// (cols, rows): the kernel holds C^T).  The kernel body is our own design:
+//
+//   warp 0 lane 0  TMA producer: W boxes for the first `stages` stages are
+//                  issued BEFORE griddepcontrol.wait (the weight does not
+//                  depend on the previous kernel), x boxes after it.
+//   warp 1 lane 0  MMA issuer: 4 x tcgen05.mma (K = 16 each) per 64-wide box,
+//                  tcgen05.commit releases the stage back to the producer.
+//   warps 0-3      epilogue: tcgen05.ld of the 128 x TOK accumulator (warp w
+//                  owns TMEM lanes 32w..32w+31 = weight rows), then either a
+//                  direct store (cluster of 1) or the cluster split-K
+//                  reduction: each CTA pushes the rows owned by peer j into
+//                  j's shared memory with st.async (counted on j's mbarrier),
+//                  and every CTA sums its ROWS/cluster rows over the cluster
+//                  in rank order (deterministic) and writes them.
+//
+// The CTAs of one cluster hold disjoint K ranges of the same 128-row tile.
+#include "device_common.cuh"
+
+namespace skg {
+
+template <int TOK, int NBOX, typename OutT, bool kFp16>
+__global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ CUtensorMap wmap,
+                                                      const __grid_constant__ CUtensorMap xmap,
+                                                      const KParams p) {
+  constexpr int ROWS = 128;
+  constexpr uint32_t kWBox = ROWS * kBoxRowBytes;
+  constexpr uint32_t kXBox = TOK * kBoxRowBytes;
+  constexpr uint32_t kStage = stage_bytes(ROWS, TOK, NBOX);
+  constexpr uint32_t kTmemCols = TOK <= 32 ? 32u : 64u;
+  constexpr uint32_t kIdesc = mma_idesc<kFp16>(ROWS, TOK);
+  static_assert(TOK % 16 == 0 && TOK >= 16 && TOK <= 64, "M=128 MMA needs N % 16 == 0");
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + kSmemAlign - 1) & ~static_cast<uint32_t>(kSmemAlign - 1);
+  uint8_t* const gbase = smem_raw + (base - raw);
+  const int S = p.stages;
+  const uint32_t red = base + static_cast<uint32_t>(S) * kStage;
+  float* const red_g = reinterpret_cast<float*>(gbase + static_cast<uint32_t>(S) * kStage);
+  const uint32_t bars = red + red_bytes(ROWS, TOK);
+  const uint32_t done_bar = bars + 8u * (2 * S);
+  const uint32_t recv_bar = done_bar + 8u;
+  const uint32_t dbg_bar = done_bar + 16u;
+  const uint32_t tmem_slot = bars + 8u * (2 * S + 4);
+  volatile uint32_t* const tmem_slot_g =
+      reinterpret_cast<volatile uint32_t*>(gbase + (tmem_slot - base));
+  auto full_bar = [&](int s) { return bars + 8u * static_cast<uint32_t>(s); };
+  auto empty_bar = [&](int s) { return bars + 8u * static_cast<uint32_t>(S + s); };
+
+  const uint32_t warp = threadIdx.x >> 5;
+  const uint32_t lane = lane_id();
+
+  if (p.debug_wait) {
+    // Watchdog self-test: wait on a barrier nothing will complete, report, return.
+    if (threadIdx.x == 0) {
+      mbar_init(dbg_bar, 1);
+      fence_mbar_init();
+    }
+    __syncthreads();
+    if (!mbar_wait_bounded(dbg_bar, 0, p.timeout_ns)) report_status(p.status, kStatusTimeoutDebug);
+    return;
+  }
+
+  const uint32_t csize = cluster_nctarank();
+  const uint32_t rank = cluster_ctarank();
+  const int n0 = static_cast<int>(blockIdx.x / csize) * ROWS;
+  const int kb0 = static_cast<int>(static_cast<int64_t>(rank) * p.kboxes / csize);
+  const int kb1 = static_cast<int>(static_cast<int64_t>(rank + 1) * p.kboxes / csize);
+  const int nb = kb1 - kb0;
+  const int iters = (nb + NBOX - 1) / NBOX;
+  const int RS = ROWS / static_cast<int>(csize);
+  const int M = p.M;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(done_bar, 1);
+    mbar_init(recv_bar, 1);
+    if (csize > 1) mbar_arrive_expect_tx(recv_bar, (csize - 1) * RS * M * 4u);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot_g;
+  if (csize > 1) cluster_arrive_release();  // matched by the wait before the pushes
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tensormap(&wmap);
+      prefetch_tensormap(&xmap);
+      const uint64_t policy = l2_policy_evict_first();
+      const int pro = iters < S ? iters : S;
+      for (int it = 0; it < pro; ++it) {
+        const int nbi = min(NBOX, nb - it * NBOX);
+        const uint32_t st = base + static_cast<uint32_t>(it) * kStage;
+        mbar_arrive_expect_tx(full_bar(it), nbi * (kWBox + kXBox));
+        for (int b = 0; b < nbi; ++b)
+          tma_load_2d_hint(st + b * kWBox, &wmap, (kb0 + it * NBOX + b) * kBoxK, n0, full_bar(it),
+                           policy);
+      }
+      pdl_wait();  // x is produced by the previous kernel on the stream
+      for (int it = 0; it < pro; ++it) {
+        const int nbi = min(NBOX, nb - it * NBOX);
+        const uint32_t st = base + static_cast<uint32_t>(it) * kStage + NBOX * kWBox;
+        for (int b = 0; b < nbi; ++b)
+          tma_load_2d(st + b * kXBox, &xmap, (kb0 + it * NBOX + b) * kBoxK, 0, full_bar(it));
+      }
+      for (int it = pro; it < iters; ++it) {
+        const int s = it % S;
+        const uint32_t ph = static_cast<uint32_t>((it / S) - 1) & 1u;
+        if (!mbar_wait_bounded(empty_bar(s), ph, p.timeout_ns))
+          report_status(p.status, kStatusTimeoutEmpty);
+        const int nbi = min(NBOX, nb - it * NBOX);
+        const uint32_t st = base + static_cast<uint32_t>(s) * kStage;
+        mbar_arrive_expect_tx(full_bar(s), nbi * (kWBox + kXBox));
+        for (int b = 0; b < nbi; ++b)
+          tma_load_2d_hint(st + b * kWBox, &wmap, (kb0 + it * NBOX + b) * kBoxK, n0, full_bar(s),
+                           policy);
+        for (int b = 0; b < nbi; ++b)
+          tma_load_2d(st + NBOX * kWBox + b * kXBox, &xmap, (kb0 + it * NBOX + b) * kBoxK, 0,
+                      full_bar(s));
+      }
+      pdl_launch_dependents();
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      pdl_wait();
+      for (int it = 0; it < iters; ++it) {
+        const int s = it % S;
+        const uint32_t ph = static_cast<uint32_t>(it / S) & 1u;
+        if (!mbar_wait_bounded(full_bar(s), ph, p.timeout_ns))
+          report_status(p.status, kStatusTimeoutFull);
+        tc_fence_after_sync();
+        const int nbi = min(NBOX, nb - it * NBOX);
+        const uint32_t wst = base + static_cast<uint32_t>(s) * kStage;
+        const uint32_t xst = wst + NBOX * kWBox;
+        for (int b = 0; b < nbi; ++b) {
+#pragma unroll
+          for (int j = 0; j < kBoxK / 16; ++j) {
+            const uint64_t ad = sw128_kmajor_desc(wst + b * kWBox + j * 32);
+            const uint64_t bd = sw128_kmajor_desc(xst + b * kXBox + j * 32);
+            tc_mma_f16kind(tmem, ad, bd, kIdesc, (it | b | j) != 0 ? 1u : 0u);
+          }
+        }
+        tc_commit(empty_bar(s));
+      }
+      tc_commit(done_bar);
+    }
+    __syncwarp();
+  }
+
+  // ------------------------------------------------------------ epilogue
+  pdl_wait();
+  if (!mbar_wait_bounded(done_bar, 0, p.timeout_ns)) report_status(p.status, kStatusTimeoutDone);
+  tc_fence_after_sync();
+  float v[TOK];
+  const uint32_t row_taddr = tmem + ((warp * 32u) << 16);
+#pragma unroll
+  for (int c = 0; c < TOK / 16; ++c) {
+    float t16[16];
+    tmem_ld_32x32b_x16(row_taddr + static_cast<uint32_t>(c * 16), t16);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[c * 16 + i] = iters > 0 ? t16[i] : 0.0f;
+  }
+  const int r = static_cast<int>(warp * 32u + lane);
+  OutT* const out = static_cast<OutT*>(p.out);
+
+  if (csize == 1) {
+    const int n = n0 + r;
+    if (n < p.N) {
+#pragma unroll
+      for (int t = 0; t < TOK; ++t)
+        if (t < M) out[static_cast<int64_t>(t) * p.ldo + n] = to_out<OutT>(v[t]);
+    }
+  } else {
+    cluster_wait_acquire();  // every peer's receive barrier is initialised
+    const uint32_t owner = static_cast<uint32_t>(r / RS);
+    const int rs = r % RS;
+    if (owner == rank) {
+#pragma unroll
+      for (int t = 0; t < TOK; ++t)
+        if (t < M) red_g[(rank * TOK + t) * RS + rs] = v[t];
+    } else {
+      const uint32_t raddr = mapa_shared(red + ((rank * TOK) * RS + rs) * 4u, owner);
+      const uint32_t rbar = mapa_shared(recv_bar, owner);
+#pragma unroll
+      for (int t = 0; t < TOK; ++t)
+        if (t < M) st_async_b32(raddr + static_cast<uint32_t>(t * RS * 4), v[t], rbar);
+    }
+    __syncthreads();
+    if (!mbar_wait_bounded<true>(recv_bar, 0, p.timeout_ns))
+      report_status(p.status, kStatusTimeoutRecv);
+    const int nbase = n0 + static_cast<int>(rank) * RS;
+    for (int idx = threadIdx.x; idx < RS * M; idx += blockDim.x) {
+      const int rs2 = idx % RS;
+      const int t = idx / RS;
+      float acc = 0.0f;
+      for (uint32_t k = 0; k < csize; ++k) acc += red_g[(k * TOK + t) * RS + rs2];
+      const int n = nbase + rs2;
+      if (n < p.N) out[static_cast<int64_t>(t) * p.ldo + n] = to_out<OutT>(acc);
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (threadIdx.x == 0) {
+    // Drain: every armed stage's last phase must have landed before exit
+    // (immediate on the normal path, where the MMA issuer waited for them).
+    const int used = iters < S ? iters : S;
+    for (int s = 0; s < used; ++s) {
+      const int last = s + ((iters - 1 - s) / S) * S;
+      if (!mbar_wait_bounded(full_bar(s), static_cast<uint32_t>(last / S) & 1u, p.timeout_ns))
+        report_status(p.status, kStatusTimeoutDrain);
+    }
+  }
+}
+
+#define SKG_TC_ENTRY(TOK, NBOX, OUTT, OUTCODE)                                              \
+  KernelEntry {                                                                             \
+    kVariantTc, 128, TOK, NBOX, 0, OUTCODE, 128,                                            \
+        reinterpret_cast<const void*>(&skinny_tc_kernel<TOK, NBOX, OUTT, false>)            \
+  }
+
+#define SKG_TC_ROW(OUTT, OUTCODE)                                                           \
+  SKG_TC_ENTRY(16, 1, OUTT, OUTCODE), SKG_TC_ENTRY(16, 2, OUTT, OUTCODE),                   \
+      SKG_TC_ENTRY(16, 4, OUTT, OUTCODE), SKG_TC_ENTRY(32, 1, OUTT, OUTCODE),               \
+      SKG_TC_ENTRY(32, 2, OUTT, OUTCODE), SKG_TC_ENTRY(32, 4, OUTT, OUTCODE),               \
+      SKG_TC_ENTRY(64, 1, OUTT, OUTCODE), SKG_TC_ENTRY(64, 2, OUTT, OUTCODE),               \
+      SKG_TC_ENTRY(64, 4, OUTT, OUTCODE)
+
+static const KernelEntry kTcTable[] = {SKG_TC_ROW(__nv_bfloat16, 0), SKG_TC_ROW(float, 2)};
+
+const KernelEntry* tc_kernel_table(int* count) {
+  *count = static_cast<int>(sizeof(kTcTable) / sizeof(kTcTable[0]));
+  return kTcTable;
+}
+
+}  // namespace skg

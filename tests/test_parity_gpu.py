@@ -1,0 +1,313 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, element
+by element, under |y - ref| <= 8e-3 |ref| + 2e-3 s (s = sqrt(sum_k (x_k w_k)^2)),
+y rounded to the output dtype.  Covers every workload at full size, every
+candidate tactic on a ragged medium shape, exact small-integer cases, tails,
+out-of-range canaries, strided views, CUDA graphs and the PDL chain."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import projection_inputs as pin
+from gpu_helpers import DEV, assert_parity, full_case, run_proj, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+def skg():
+    import skinny_bf16_projection_gb300 as m
+    return m
+
+
+# ------------------------------------------------------------------ workloads
+def test_tiny_config():
+    w, x, ref, s = full_case(1536, 128)
+    proj = skg().Projection(w.to(DEV))
+    y = run_proj(proj, x[:1].to(DEV), torch.bfloat16)
+    assert_parity(y, ref[:1], s[:1], f"tiny M=1 {proj.plan(1)}")
+    proj.check_status()
+
+
+@pytest.mark.parametrize("N", [3584, 6288])
+def test_decode_projection_sweep_one_handle(N):
+    """One weight and one handle across M = 1..32: exercises the per-M plan."""
+    w, x, ref, s = full_case(N, 7168)
+    proj = skg().Projection(w.to(DEV))
+    xd = x.to(DEV)
+    for M in (1, 2, 4, 8, 16, 32):
+        y = run_proj(proj, xd[:M], torch.bfloat16)
+        assert_parity(y, ref[:M], s[:M], f"N={N} M={M} {proj.plan(M)}")
+    proj.check_status()
+
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("N", [3584, 6288])
+def test_split_k_token_tiles(N, out_dtype):
+    w, x, ref, s = full_case(N, 7168)
+    proj = skg().Projection(w.to(DEV), out_dtype)
+    xd = x.to(DEV)
+    for M in (4, 8, 16, 32, 48, 64):
+        y = run_proj(proj, xd[:M], out_dtype)
+        assert_parity(y, ref[:M], s[:M], f"N={N} M={M} {out_dtype} {proj.plan(M)}")
+    assert proj.plan(48).split(":")[2] == "t64"  # M=48 runs on the 64-token tile
+    proj.check_status()
+
+
+# ------------------------------------------------------------------ every tactic
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_every_candidate_tactic_on_ragged_shape(out_dtype):
+    # 656 rows = 5 tiles of 128 + 16 (or 10 of 64 + 16); 17 K blocks split
+    # unevenly over every cluster size; K = 1088 = 17 * 64.
+    N, K = 656, 1088
+    w, x, ref, s = full_case(N, K, seed=3)
+    proj = skg().Projection(w.to(DEV), out_dtype, use_tactic_file=False)
+    xd = x.to(DEV)
+    seen = set()
+    for M in (1, 3, 8, 13, 16, 31, 48, 64):
+        cands = proj.tactics(M)
+        assert cands, f"no candidates at M={M}"
+        for t in cands:
+            proj.set_tactic(M, t)
+            y = run_proj(proj, xd[:M], out_dtype)
+            assert_parity(y, ref[:M], s[:M], f"M={M} {t}")
+            seen.add(t.split(":s")[0])
+    proj.check_status()
+    assert any(t.startswith("tc:") for t in seen) and any(t.startswith("mma:") for t in seen)
+
+
+def test_small_integers_exact_for_every_tactic():
+    """Integer inputs make every partial sum exact in fp32, whatever the split:
+    fp32 output must equal the oracle bit for bit, bf16 output its rounding."""
+    N, K = 320, 2048
+    w = pin.small_integers(N, K, seed=21)
+    x = pin.small_integers(64, K, seed=22)
+    ref, _ = oracle.projection(x, w, with_scale=False)
+    want_bf16 = oracle.round_bf16(ref)
+    wd, xd = w.to(DEV), x.to(DEV)
+    p32 = skg().Projection(wd, torch.float32, use_tactic_file=False)
+    p16 = skg().Projection(wd, torch.bfloat16, use_tactic_file=False)
+    for M in (1, 8, 24, 64):
+        for t in p32.tactics(M):
+            p32.set_tactic(M, t)
+            p16.set_tactic(M, t)
+            y32 = run_proj(p32, xd[:M], torch.float32)
+            y16 = run_proj(p16, xd[:M], torch.bfloat16)
+            assert np.array_equal(to_f64(y32), ref[:M]), f"fp32 not exact: M={M} {t}"
+            got16 = y16.cpu().view(torch.int16).numpy().view(np.uint16)
+            assert np.array_equal(got16, want_bf16[:M]), f"bf16 not RNE of exact: M={M} {t}"
+
+
+def test_bf16_output_is_rounding_of_fp32_output_same_tactic():
+    w, x, ref, s = full_case(3584, 7168)
+    wd, xd = w.to(DEV), x.to(DEV)
+    p32 = skg().Projection(wd, torch.float32, use_tactic_file=False)
+    p16 = skg().Projection(wd, torch.bfloat16, use_tactic_file=False)
+    for M in (1, 16, 64):
+        p16.set_tactic(M, p32.plan(M))
+        y32 = run_proj(p32, xd[:M], torch.float32)
+        y16 = run_proj(p16, xd[:M], torch.bfloat16)
+        assert torch.equal(y32.to(torch.bfloat16), y16), f"M={M}"
+
+
+def test_deterministic_bits():
+    w, x, _, _ = full_case(6288, 7168)
+    proj = skg().Projection(w.to(DEV))
+    xd = x.to(DEV)
+    for M in (1, 32, 64):
+        a = run_proj(proj, xd[:M], torch.bfloat16)
+        b = run_proj(proj, xd[:M], torch.bfloat16)
+        assert torch.equal(a, b)
+
+
+# ------------------------------------------------------------------ tails / bounds
+@pytest.mark.parametrize("N,K", [(16, 64), (48, 128), (6296, 7168), (100, 7232), (130, 72),
+                                 (257, 200), (1, 8), (129, 7168 + 64)])
+def test_tails(N, K):
+    w, x, ref, s = full_case(N, K, seed=5)
+    for odt in (torch.bfloat16, torch.float32):
+        proj = skg().Projection(w.to(DEV), odt, use_tactic_file=False)
+        for M in (1, 5, 33, 64):
+            y = run_proj(proj, x[:M].to(DEV), odt)
+            assert_parity(y, ref[:M], s[:M], f"N={N} K={K} M={M} {odt} {proj.plan(M)}")
+
+
+@pytest.mark.parametrize("odt", [torch.bfloat16, torch.float32])
+def test_canaries_rows_cols_untouched_and_padding_never_read(odt):
+    N, K = 3584, 7168
+    w, x, ref, s = full_case(N, K)
+    proj = skg().Projection(w.to(DEV), odt, use_tactic_file=False)
+    for M in (1, 7, 48):
+        xbuf = torch.full((64, K), float("nan"), dtype=torch.bfloat16, device=DEV)
+        xbuf[:M] = x[:M].to(DEV)
+        obuf = torch.full((M + 3, N + 16), float("nan"), dtype=odt, device=DEV)
+        out = obuf[:M, :N]
+        proj.run(xbuf[:M], out)
+        torch.cuda.synchronize()
+        assert torch.isnan(obuf[M:]).all(), "rows >= M were written"
+        assert torch.isnan(obuf[:, N:]).all(), "columns >= N were written"
+        assert torch.isfinite(out).all(), "x rows >= M were read (NaN poison leaked)"
+        assert_parity(out, ref[:M], s[:M], f"canary M={M}")
+
+
+def test_strided_views():
+    N, K = 1000, 1024
+    w, x, ref, s = full_case(N, K, seed=7)
+    wide_w = torch.zeros((N, K + 128), dtype=torch.bfloat16)
+    wide_w[:, 64:64 + K] = w
+    wide_w = wide_w.to(DEV)
+    wv = wide_w[:, 64:64 + K]  # row pitch K+128, 128-byte offset
+    proj = skg().Projection(wv)
+    xw = torch.zeros((64, K + 64), dtype=torch.bfloat16, device=DEV)
+    xw[:, 8:8 + K] = x.to(DEV)
+    ow = torch.zeros((64, N + 8), dtype=torch.bfloat16, device=DEV)
+    for M in (1, 9, 64):
+        proj.run(xw[:M, 8:8 + K], ow[:M, :N])
+        assert_parity(ow[:M, :N], ref[:M], s[:M], f"strided M={M}")
+
+
+# ------------------------------------------------------------------ graphs / PDL
+def test_graph_capture_replay_all_token_counts():
+    w, x, ref, s = full_case(3584, 7168)
+    proj = skg().Projection(w.to(DEV))
+    xd = x.to(DEV)
+    Ms = (1, 2, 4, 8, 16, 32, 48, 64)
+    outs = {M: torch.empty((M, 3584), dtype=torch.bfloat16, device=DEV) for M in Ms}
+    eager = {}
+    for M in Ms:
+        proj.run(xd[:M], outs[M])
+        eager[M] = outs[M].clone()
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for M in Ms:
+            proj.run(xd[:M], outs[M])
+    for M in Ms:
+        outs[M].zero_()
+    for _ in range(20):
+        g.replay()
+    torch.cuda.synchronize()
+    for M in Ms:
+        assert torch.equal(outs[M], eager[M]), f"graph replay differs at M={M}"
+        assert_parity(outs[M], ref[:M], s[:M], f"graph M={M}")
+
+
+def test_pdl_chain_of_dependent_projections():
+    """8 projections where each output is the next input (N == K): back-to-back
+    launches with programmatic dependent launch must still see the previous
+    output; each link is checked against the oracle on the GPU's own input."""
+    D = 2048
+    w = pin.weight(D, D, seed=9, std=1.0 / np.sqrt(D))
+    x0 = pin.case(8, D, seed=10)[1]
+    proj = skg().Projection(w.to(DEV), use_tactic_file=False)
+    for M in (1, 16):
+        bufs = [x0[:M].to(DEV)] + [torch.empty((M, D), dtype=torch.bfloat16, device=DEV)
+                                   for _ in range(8)]
+        for i in range(8):
+            proj.run(bufs[i], bufs[i + 1])
+        torch.cuda.synchronize()
+        for i in range(8):
+            ref, s = oracle.projection(bufs[i].cpu(), w)
+            assert_parity(bufs[i + 1], ref, s, f"chain link {i} M={M}")
+
+
+# ------------------------------------------------------------------ host API paths
+def test_run_host_end_to_end():
+    w, x, ref, s = full_case(3584, 7168)
+    proj = skg().Projection(w.to(DEV))
+    for M in (1, 32):
+        xh = x[:M].contiguous().pin_memory()
+        oh = torch.empty((M, 3584), dtype=torch.bfloat16).pin_memory()
+        proj.run_host(xh, oh)
+        assert_parity(oh, ref[:M], s[:M], f"run_host M={M}")
+
+
+def test_autotune_installs_a_valid_plan():
+    w, x, ref, s = full_case(3584, 7168)
+    proj = skg().Projection(w.to(DEV), use_tactic_file=False)
+    proj.autotune([1, 8, 32])
+    xd = x.to(DEV)
+    for M in (1, 2, 5, 8, 20, 32, 64):
+        plan = proj.plan(M)
+        y = run_proj(proj, xd[:M], torch.bfloat16)
+        assert_parity(y, ref[:M], s[:M], f"tuned M={M} {plan}")
+    assert proj.plan(5) == proj.plan(8)  # untuned M take the next tuned M's tactic
+
+
+def test_watchdog_reports_timeout_and_recovers():
+    import skinny_bf16_projection_gb300 as m
+    w, x, ref, s = full_case(1536, 128)
+    proj = m.Projection(w.to(DEV))
+    proj.inject_timeout(1, 2_000_000)  # next launch waits 2 ms on a dead barrier
+    out = torch.zeros((1, 1536), dtype=torch.bfloat16, device=DEV)
+    proj.run(x[:1].to(DEV), out)
+    with pytest.raises(m.SkinnyGemmError) as e:
+        proj.check_status()
+    assert e.value.code == m._native.SKG_ETIMEOUT
+    proj.check_status()  # cleared
+    y = run_proj(proj, x[:1].to(DEV), torch.bfloat16)
+    assert_parity(y, ref[:1], s[:1], "after watchdog")
+
+
+def test_error_codes():
+    import skinny_bf16_projection_gb300 as m
+    nat = m._native
+    lib = nat.lib()
+    w = torch.randn(256, 1024, device=DEV).to(torch.bfloat16)
+    proj = m.Projection(w)
+    x = torch.randn(64, 1024 + 8, device=DEV).to(torch.bfloat16)
+    out = torch.empty(64, 256 + 8, device=DEV, dtype=torch.bfloat16)
+    st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert lib.skinny_gemm_run(proj._h, x.data_ptr(), 0, out.data_ptr(), st) == nat.SKG_EUNSUPPORTED_M
+    assert lib.skinny_gemm_run(proj._h, x.data_ptr(), 65, out.data_ptr(), st) == nat.SKG_EUNSUPPORTED_M
+    assert lib.skinny_gemm_run(proj._h, x.data_ptr() + 2, 4, out.data_ptr(), st) == nat.SKG_EALIGN
+    assert lib.skinny_gemm_run(proj._h, x.data_ptr(), 4, out.data_ptr() + 8, st) == nat.SKG_EALIGN
+    assert lib.skinny_gemm_run_strided(proj._h, x.data_ptr(), 1000, 4, out.data_ptr(), 256, st) \
+        == nat.SKG_EINVAL  # ldx < K
+    assert lib.skinny_gemm_run_strided(proj._h, x.data_ptr(), 1028, 4, out.data_ptr(), 256, st) \
+        == nat.SKG_EALIGN  # ldx * 2 not a 16-byte multiple
+    assert lib.skinny_gemm_prepare(w.data_ptr() + 2, 256, 1024, 0, 0) is None
+    assert lib.skinny_gemm_last_status() == nat.SKG_EALIGN
+    assert lib.skinny_gemm_prepare(w.data_ptr(), 256, 1024, 0, 1) is None
+    assert lib.skinny_gemm_last_status() == nat.SKG_EINVAL
+    with pytest.raises(m.SkinnyGemmError):
+        proj.set_tactic(40, "tc:r128:t32:b2:s4:c1")  # token tile 32 < M = 40
+    with pytest.raises(m.SkinnyGemmError):
+        proj.set_tactic(8, "tc:r128:t16:b2:s4:c32")  # cluster size 32 is not offered
+    with pytest.raises(m.SkinnyGemmError):
+        proj.set_tactic(8, "bogus")
+    with pytest.raises(ValueError):
+        proj.run(x[:4, :1024], torch.empty(4, 255, device=DEV, dtype=torch.bfloat16))
+    torch.cuda.synchronize()
+
+
+def test_autotune_refuses_during_capture():
+    import skinny_bf16_projection_gb300 as m
+    nat = m._native
+    lib = nat.lib()
+    w = torch.randn(256, 1024, device=DEV).to(torch.bfloat16)
+    proj = m.Projection(w)
+    s = torch.cuda.Stream()
+    arr = (ctypes.c_int64 * 1)(8)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    codes = {}
+    # relaxed mode: the refused calls do not invalidate the capture
+    with torch.cuda.graph(g, stream=s, capture_error_mode="relaxed"):
+        codes["autotune"] = lib.skinny_gemm_autotune(proj._h, arr, 1, ctypes.c_void_p(s.cuda_stream))
+        y = torch.empty(8, 256, device=DEV, dtype=torch.bfloat16)
+        x = torch.zeros(8, 1024, device=DEV, dtype=torch.bfloat16)
+        proj.run(x, y, stream=s)
+    assert codes["autotune"] == nat.SKG_ECAPTURING
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(y) == 0
