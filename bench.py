@@ -47,7 +47,7 @@ def kernel_source_hash() -> str:
     csrc = os.path.join(ROOT, "skinny_bf16_projection_gb300", "csrc")
     h = hashlib.sha256()
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
+        if name.startswith("kernel") or name == "device_common.cuh":
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
