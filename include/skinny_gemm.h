@@ -176,6 +176,42 @@ int skinny_gemm_debug_inject_timeout(skinny_gemm_t h, int count, uint64_t timeou
  * make sure no launch using it is still pending.  NULL is ignored. */
 void skinny_gemm_destroy(skinny_gemm_t h);
 
+/*
+ * One projection with NO allocation and no handle: out[M, N] = x[M, K] @ W^T.
+ * (The pages have no counterpart; this entry point is this library's own.)
+ *
+ * For callers that cannot allocate device memory: code that runs while a
+ * stream is being captured in global mode (where cudaMalloc is refused and
+ * spoils the capture), serving engines that hand all of HBM to their own
+ * pool allocator up front, and code that must not risk the device-wide
+ * synchronization cudaMalloc/cudaFree may imply.  skinny_gemm_prepare
+ * allocates a device status word, so such callers use this function instead.
+ *
+ * Arguments: W [N, K] with row pitch ldw, x [M, K] with pitch ldx, out [M, N]
+ * with pitch ldo, all DEVICE pointers on the current device (same alignment
+ * rules as skinny_gemm_prepare_ex / skinny_gemm_run_strided); out_dtype
+ * SKG_BF16 or SKG_FP32; weights and inputs bf16.  Uses the untuned default
+ * tactic for (N, K, M).
+ *
+ * Scratch: the kernels' one piece of scratch, the 4-byte watchdog status word,
+ * lives in a static 256-byte device array inside the library (held on every
+ * GPU that loads the library until the process exits).  A request needing more
+ * scratch than 256 bytes is rejected with SKG_EINVAL and a message.  Each call
+ * clears the word on `stream` before its launch; the word is not read back
+ * (use the handle API for watchdog reports).  All calls share the array, so
+ * calls that overlap on the GPU (different streams, or different host threads)
+ * race on it; serialize them on one stream.
+ *
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call before any stream capture.  Calls no cudaMalloc, cudaFree or
+ * other allocating routine.  Asynchronous: returns after the launch.
+ * Errors: EINVAL, EALIGN, EUNSUPPORTED_M, EDEVICE, ECUDA.
+ */
+int skinny_gemm_run_noalloc(const void* W, int64_t N, int64_t K, int64_t ldw, int out_dtype,
+                            const void* x, int64_t ldx, int64_t M, void* out, int64_t ldo,
+                            void* stream);
+
 /* Thread-local description of the last failure on this thread ("" if none). */
 const char* skinny_gemm_last_error(void);
 

@@ -799,3 +799,87 @@ void skinny_gemm_destroy(skinny_gemm_t h) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ no-allocation entry point
+// skinny_gemm_run_noalloc is for callers that cannot allocate device memory
+// (see its declaration in skinny_gemm.h).  The only scratch the kernels need
+// is the watchdog status word; here it lives in this file-scope array instead
+// of a cudaMalloc'd word owned by a handle.  Every GPU that loads the library
+// holds these 256 bytes until the process exits.
+namespace {
+constexpr size_t kNoAllocScratchBytes = 256;
+}  // namespace
+
+static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocScratchBytes / sizeof(uint32_t)];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+uint32_t* g_noalloc_addr[64] = {};
+
+// Device address of the scratch array on device `dev` (which must be current).
+// Host code cannot pass `g_noalloc_scratch` itself to a kernel: on the host
+// that name is a stand-in, not a device address.  Looked up once per device.
+int noalloc_scratch_address(int dev, uint32_t** out) {
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-alloc scratch)");
+    g_noalloc_addr[dev] = static_cast<uint32_t*>(p);
+  }
+  *out = g_noalloc_addr[dev];
+  return SKG_OK;
+}
+
+}  // namespace
+
+extern "C" int skinny_gemm_run_noalloc(const void* W, int64_t N, int64_t K, int64_t ldw,
+                                       int out_dtype, const void* x, int64_t ldx, int64_t M,
+                                       void* out, int64_t ldo, void* stream) {
+  if (W == nullptr) return fail(SKG_EINVAL, "null weight pointer");
+  if (out_dtype != SKG_BF16 && out_dtype != SKG_FP32)
+    return fail(SKG_EINVAL, "unsupported projection output dtype %d (BF16 or FP32)", out_dtype);
+  if (N < 1 || K < 8 || N > (1ll << 31) - 1 || K > (1ll << 31) - 1)
+    return fail(SKG_EINVAL, "weight shape [%lld, %lld] out of range", static_cast<long long>(N),
+                static_cast<long long>(K));
+  if (K % 8 != 0 || ldw < K || ldw % 8 != 0 || reinterpret_cast<uintptr_t>(W) % 16 != 0)
+    return fail(SKG_EALIGN, "weight rows need a 16-byte aligned base and pitch (K %% 8 == 0)");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  DeviceInfo* di = nullptr;
+  if (device_info(dev, &di) != SKG_OK) return g_last_status;
+  uint32_t* scratch = nullptr;
+  if (noalloc_scratch_address(dev, &scratch) != SKG_OK) return g_last_status;
+
+  // A plan on the stack (host memory, gone at return): no handle, no allocation.
+  skinny_gemm_plan p;
+  p.W = W;
+  p.N = N;
+  p.K = K;
+  p.ldw = ldw;
+  p.dtype = SKG_BF16;
+  p.out_dtype = out_dtype;
+  p.device = dev;
+  p.dev = di;
+  p.kboxes = static_cast<int>((K + kBoxK - 1) / kBoxK);
+  p.status = scratch;
+  p.timeout_ns = env_u64("SKINNY_GEMM_TIMEOUT_NS", 2000000000ull);
+  int rc = validate_run(&p, x, ldx, M, out, ldo);
+  if (rc != SKG_OK) return rc;
+  const Tactic t = default_tactic(&p, M);
+  if (!t.valid()) return fail(SKG_EINVAL, "no valid tactic for M = %lld", static_cast<long long>(M));
+  const size_t need = sizeof(uint32_t);  // the launched kernels' scratch: one status word
+  if (need > kNoAllocScratchBytes)
+    return fail(SKG_EINVAL, "needs %zu bytes of scratch, more than the %zu-byte static buffer", need,
+                kNoAllocScratchBytes);
+  rc = encode_map(t.rows == 64 ? &p.wmap64 : &p.wmap128, W, N, K, ldw, t.rows, SKG_BF16,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+  if (rc != SKG_OK) return rc;
+  // The array keeps the previous call's contents: the status word must start at zero.
+  e = cudaMemsetAsync(scratch, 0, need, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(no-alloc scratch)");
+  rc = launch_tactic(&p, t, x, ldx, M, out, ldo, static_cast<cudaStream_t>(stream));
+  return rc == SKG_OK ? ok() : rc;
+}
