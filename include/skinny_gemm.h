@@ -140,12 +140,15 @@ int skinny_gemm_run_overlap(skinny_gemm_t h_main, skinny_gemm_t h_fa, skinny_gem
 /*
  * Time the candidate tactics for each M in Ms[0..nM) on this GPU and install
  * the fastest in the plan; M values not listed take the tuned tactic of the
- * smallest listed M' >= M that shares their token tile, else keep the default
- * (low_latency_gemm page, autotune_kda_qkvg: autotune before CUDA graph
- * capture).  Synchronizes `stream`; allocates and frees a temporary L2-flush
- * buffer; writes garbage into nothing the caller owns.  Must not be called
- * while capturing (ECAPTURING).  When SKINNY_GEMM_TACTIC_FILE names a file,
- * results are appended there and reused by later prepares.
+ * smallest listed M' >= M, else keep the default (low_latency_gemm page,
+ * autotune_kda_qkvg: autotune before CUDA graph capture).  Each candidate is
+ * timed as a CUDA graph of back-to-back launches that rotate over scratch
+ * copies of the weight's layout (>= 2x the L2 size, so reads come from HBM),
+ * i.e. in the steady state of a decode step.  Synchronizes `stream`;
+ * allocates and frees those copies; may grow the handle's workspace; writes
+ * nothing the caller owns.  Must not be called while capturing (ECAPTURING).
+ * When SKINNY_GEMM_TACTIC_FILE names a file, results are appended there and
+ * reused by later prepares.
  */
 int skinny_gemm_autotune(skinny_gemm_t h, const int64_t* Ms, int nM, void* stream);
 

@@ -106,23 +106,28 @@ struct Tactic {
   bool valid() const { return variant != 0; }
 };
 
+// "tc:r128:t16:b2:s4:c8" (c = cluster size) or "sk:r128:t16:b2:s5:g1" (g = CTAs per SM).
 std::string tactic_str(const Tactic& t) {
   char b[96];
-  snprintf(b, sizeof b, "%s:r%d:t%d:b%d:s%d:c%d", t.variant == kVariantTc ? "tc" : "mma", t.rows,
-           t.tok, t.nbox, t.stages, t.cl);
+  const char* kind = t.variant == kVariantTc ? "tc" : (t.variant == kVariantSk ? "sk" : "mma");
+  snprintf(b, sizeof b, "%s:r%d:t%d:b%d:s%d:%c%d", kind, t.rows, t.tok, t.nbox, t.stages,
+           t.variant == kVariantSk ? 'g' : 'c', t.cl);
   return b;
 }
 
 bool tactic_parse(const char* s, Tactic* t) {
   char kind[16] = {0};
+  char last = 0;
   Tactic x;
-  if (s == nullptr ||
-      sscanf(s, "%15[^:]:r%d:t%d:b%d:s%d:c%d", kind, &x.rows, &x.tok, &x.nbox, &x.stages, &x.cl) != 6)
+  if (s == nullptr || sscanf(s, "%15[^:]:r%d:t%d:b%d:s%d:%c%d", kind, &x.rows, &x.tok, &x.nbox,
+                             &x.stages, &last, &x.cl) != 7)
     return false;
-  if (strcmp(kind, "tc") == 0)
+  if (strcmp(kind, "tc") == 0 && last == 'c')
     x.variant = kVariantTc;
-  else if (strcmp(kind, "mma") == 0)
+  else if (strcmp(kind, "mma") == 0 && last == 'c')
     x.variant = kVariantMma;
+  else if (strcmp(kind, "sk") == 0 && last == 'g')
+    x.variant = kVariantSk;
   else
     return false;
   *t = x;
@@ -131,7 +136,9 @@ bool tactic_parse(const char* s, Tactic* t) {
 
 const KernelEntry* find_kernel(const Tactic& t, int in_dtype, int out_dtype) {
   int n = 0;
-  const KernelEntry* tab = t.variant == kVariantTc ? tc_kernel_table(&n) : mma_kernel_table(&n);
+  const KernelEntry* tab = t.variant == kVariantTc   ? tc_kernel_table(&n)
+                           : t.variant == kVariantSk ? sk_kernel_table(&n)
+                                                     : mma_kernel_table(&n);
   for (int i = 0; i < n; ++i)
     if (tab[i].rows == t.rows && tab[i].tok == t.tok && tab[i].nbox == t.nbox &&
         tab[i].in_dtype == in_dtype && tab[i].out_dtype == out_dtype)
@@ -145,6 +152,8 @@ std::vector<const KernelEntry*> all_kernels() {
   const KernelEntry* a = tc_kernel_table(&n);
   for (int i = 0; i < n; ++i) v.push_back(&a[i]);
   a = mma_kernel_table(&n);
+  for (int i = 0; i < n; ++i) v.push_back(&a[i]);
+  a = sk_kernel_table(&n);
   for (int i = 0; i < n; ++i) v.push_back(&a[i]);
   return v;
 }
@@ -210,6 +219,10 @@ struct skinny_gemm_plan {
   CUtensorMap wmap64{}, wmap128{};
   Tactic plan[SKINNY_GEMM_MAX_M + 1];
   uint32_t* status = nullptr;
+  float* workspace = nullptr;      // stream-K partial sums (allocated when a tactic needs it)
+  size_t workspace_bytes = 0;
+  uint32_t* counters = nullptr;    // stream-K per-tile arrival counters, zero between launches
+  size_t counters_bytes = 0;
   void* x_stage = nullptr;
   void* out_stage = nullptr;
   uint64_t timeout_ns = 2000000000ull;
@@ -221,6 +234,31 @@ namespace {
 
 int out_elem_bytes(const skinny_gemm_plan* h) { return h->out_dtype == SKG_FP32 ? 4 : 2; }
 
+int ntiles_of(const skinny_gemm_plan* h, const Tactic& t) {
+  return static_cast<int>((h->N + t.rows - 1) / t.rows);
+}
+uint32_t tactic_smem(const Tactic& t) {
+  return t.variant == kVariantSk ? sk_smem_bytes(t.tok, t.nbox, t.stages)
+                                 : smem_bytes(t.rows, t.tok, t.nbox, t.stages);
+}
+// CTAs launched: row tiles x cluster size, or (stream-K) CTAs-per-SM x SMs,
+// capped at the number of work units.
+int tactic_grid(const skinny_gemm_plan* h, const Tactic& t) {
+  if (t.variant != kVariantSk) return ntiles_of(h, t) * t.cl;
+  const int64_t units = static_cast<int64_t>(ntiles_of(h, t)) * h->kboxes;
+  return static_cast<int>(std::min<int64_t>(static_cast<int64_t>(t.cl) * h->dev->sm_count, units));
+}
+int tactic_cluster(const Tactic& t) { return t.variant == kVariantSk ? 1 : t.cl; }
+// Stream-K scratch: two fp32 [TOK][128] partial-sum slots per CTA, one counter per tile.
+void workspace_need(const skinny_gemm_plan* h, const Tactic& t, size_t* ws, size_t* cnt) {
+  if (t.variant != kVariantSk) {
+    *ws = *cnt = 0;
+    return;
+  }
+  *ws = static_cast<size_t>(tactic_grid(h, t)) * 2 * t.tok * t.rows * sizeof(float);
+  *cnt = static_cast<size_t>(ntiles_of(h, t)) * sizeof(uint32_t);
+}
+
 // Validity of tactic t for this weight at token count M (M = 0: any M <= tok).
 bool tactic_fits(const skinny_gemm_plan* h, const Tactic& t, int64_t M, std::string* why) {
   auto no = [&](const char* w) {
@@ -231,21 +269,62 @@ bool tactic_fits(const skinny_gemm_plan* h, const Tactic& t, int64_t M, std::str
   const KernelEntry* k = find_kernel(t, h->dtype, h->out_dtype);
   if (k == nullptr) return no("no compiled kernel for this rows/tok/box/dtype combination");
   if (M > t.tok) return no("token tile smaller than M");
-  bool pow2 = false;
-  for (int c : kClusters) pow2 |= (c == t.cl);
-  if (!pow2) return no("cluster size must be 1, 2, 4, 8 or 16");
-  if (t.cl > h->kboxes) return no("cluster larger than the number of 64-wide K blocks");
-  if (t.rows % t.cl != 0) return no("cluster size must divide the row tile");
+  if (t.variant == kVariantSk) {
+    if (t.cl != 1 && t.cl != 2) return no("stream-K runs 1 or 2 CTAs per SM");
+  } else {
+    bool pow2 = false;
+    for (int c : kClusters) pow2 |= (c == t.cl);
+    if (!pow2) return no("cluster size must be 1, 2, 4, 8 or 16");
+    if (t.cl > h->kboxes) return no("cluster larger than the number of 64-wide K blocks");
+    if (t.rows % t.cl != 0) return no("cluster size must divide the row tile");
+  }
   if (t.stages < 1 || t.stages > 16) return no("stages out of range 1..16");
-  if (static_cast<int>(smem_bytes(t.rows, t.tok, t.nbox, t.stages)) > h->dev->smem_optin)
+  if (static_cast<int>(tactic_smem(t)) > h->dev->smem_optin)
     return no("shared memory footprint exceeds the per-block limit");
   return true;
+}
+
+// Grow the handle's stream-K workspace and counters to fit tactic t.  Only
+// called from prepare / set_tactic / autotune (never from run): it may
+// synchronize the device and allocate.
+int ensure_workspace(skinny_gemm_plan* h, const Tactic& t) {
+  size_t ws = 0, cnt = 0;
+  workspace_need(h, t, &ws, &cnt);
+  if (ws <= h->workspace_bytes && cnt <= h->counters_bytes) return SKG_OK;
+  cudaError_t e = cudaDeviceSynchronize();  // no launch may still use the old buffers
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  if (ws > h->workspace_bytes) {
+    if (h->workspace) cudaFree(h->workspace);
+    h->workspace = nullptr;
+    h->workspace_bytes = 0;
+    e = cudaMalloc(&h->workspace, ws);
+    if (e != cudaSuccess) return h->workspace = nullptr, cuda_fail(e, "cudaMalloc(workspace)");
+    h->workspace_bytes = ws;
+  }
+  if (cnt > h->counters_bytes) {
+    if (h->counters) cudaFree(h->counters);
+    h->counters = nullptr;
+    h->counters_bytes = 0;
+    e = cudaMalloc(&h->counters, cnt);
+    if (e != cudaSuccess) return h->counters = nullptr, cuda_fail(e, "cudaMalloc(counters)");
+    e = cudaMemset(h->counters, 0, cnt);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(counters)");
+    h->counters_bytes = cnt;
+  }
+  return SKG_OK;
 }
 
 int launch_tactic(skinny_gemm_plan* h, const Tactic& t, const void* x, int64_t ldx, int64_t M,
                   void* out, int64_t ldo, cudaStream_t st) {
   const KernelEntry* k = find_kernel(t, h->dtype, h->out_dtype);
   if (k == nullptr) return fail(SKG_EINVAL, "no kernel for tactic %s", tactic_str(t).c_str());
+  if (t.variant == kVariantSk) {
+    size_t ws = 0, cnt = 0;
+    workspace_need(h, t, &ws, &cnt);
+    if (ws > h->workspace_bytes || cnt > h->counters_bytes)
+      return fail(SKG_EINVAL, "tactic %s needs a workspace this handle has not prepared",
+                  tactic_str(t).c_str());
+  }
   CUtensorMap xmap;
   int rc = encode_map(&xmap, x, M, h->K, ldx, t.tok, h->dtype, CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
   if (rc != SKG_OK) return rc;
@@ -258,20 +337,21 @@ int launch_tactic(skinny_gemm_plan* h, const Tactic& t, const void* x, int64_t l
   p.stages = t.stages;
   p.status = h->status;
   p.timeout_ns = h->timeout_ns;
+  p.workspace = h->workspace;
+  p.counters = h->counters;
   if (h->debug_count > 0) {
     --h->debug_count;
     p.debug_wait = 1;
     p.timeout_ns = h->debug_timeout_ns;
   }
-  const int ntiles = static_cast<int>((h->N + t.rows - 1) / t.rows);
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(static_cast<unsigned>(ntiles * t.cl), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(tactic_grid(h, t)), 1, 1);
   cfg.blockDim = dim3(static_cast<unsigned>(k->threads), 1, 1);
-  cfg.dynamicSmemBytes = smem_bytes(t.rows, t.tok, t.nbox, t.stages);
+  cfg.dynamicSmemBytes = tactic_smem(t);
   cfg.stream = st;
   cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeClusterDimension;
-  attrs[0].val.clusterDim.x = static_cast<unsigned>(t.cl);
+  attrs[0].val.clusterDim.x = static_cast<unsigned>(tactic_cluster(t));
   attrs[0].val.clusterDim.y = 1;
   attrs[0].val.clusterDim.z = 1;
   attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -290,13 +370,12 @@ int active_clusters(const skinny_gemm_plan* h, const Tactic& t) {
   const KernelEntry* k = find_kernel(t, h->dtype, h->out_dtype);
   if (k == nullptr) return 0;
   cudaLaunchConfig_t cfg{};
-  const int ntiles = static_cast<int>((h->N + t.rows - 1) / t.rows);
-  cfg.gridDim = dim3(static_cast<unsigned>(ntiles * t.cl), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(tactic_grid(h, t)), 1, 1);
   cfg.blockDim = dim3(static_cast<unsigned>(k->threads), 1, 1);
-  cfg.dynamicSmemBytes = smem_bytes(t.rows, t.tok, t.nbox, t.stages);
+  cfg.dynamicSmemBytes = tactic_smem(t);
   cudaLaunchAttribute a[1];
   a[0].id = cudaLaunchAttributeClusterDimension;
-  a[0].val.clusterDim.x = static_cast<unsigned>(t.cl);
+  a[0].val.clusterDim.x = static_cast<unsigned>(tactic_cluster(t));
   a[0].val.clusterDim.y = 1;
   a[0].val.clusterDim.z = 1;
   cfg.attrs = a;
@@ -313,8 +392,8 @@ int active_clusters(const skinny_gemm_plan* h, const Tactic& t) {
 // every stage count / box count / cluster size that fits and can launch.
 std::vector<Tactic> candidates(const skinny_gemm_plan* h, int64_t M) {
   std::vector<Tactic> out;
-  for (int variant : {kVariantTc, kVariantMma}) {
-    const int* toks = variant == kVariantTc ? kTcToks : kMmaToks;
+  for (int variant : {kVariantTc, kVariantMma, kVariantSk}) {
+    const int* toks = variant == kVariantMma ? kMmaToks : kTcToks;
     int tok = 0;
     for (int i = 0; i < 3; ++i)
       if (toks[i] >= M) {
@@ -331,6 +410,8 @@ std::vector<Tactic> candidates(const skinny_gemm_plan* h, int64_t M) {
           Tactic t{variant, k->rows, tok, k->nbox, s, cl};
           if (!tactic_fits(h, t, M, nullptr)) continue;
           if (active_clusters(h, t) <= 0) continue;
+          // stream-K: every CTA of the grid must be resident at once (one wave)
+          if (variant == kVariantSk && active_clusters(h, t) < tactic_grid(h, t)) continue;
           out.push_back(t);
         }
     }
@@ -413,17 +494,6 @@ void append_tactic_file(const skinny_gemm_plan* h, int64_t M, const Tactic& t, d
   fprintf(f, "%s %lld %s %.3f\n", cache_key(h).c_str(), static_cast<long long>(M),
           tactic_str(t).c_str(), us);
   fclose(f);
-}
-
-// ------------------------------------------------------------------ L2 flush (autotuner)
-__global__ void l2_flush_kernel(const uint4* __restrict__ buf, size_t n, uint32_t* sink) {
-  uint32_t acc = 0;
-  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const uint4 v = __ldcs(buf + i);
-    acc ^= v.x ^ v.y ^ v.z ^ v.w;
-  }
-  if (acc == 0x9E3779B9u && sink != nullptr) *sink = acc;  // keeps the loads alive
 }
 
 int check_handle(const skinny_gemm_plan* h) {
@@ -526,12 +596,20 @@ skinny_gemm_t skinny_gemm_prepare_ex(const void* W, int64_t N, int64_t K, int64_
       for (int m = 1; m <= SKINNY_GEMM_MAX_M; ++m)
         if (tactic_fits(h, t, m, nullptr)) h->plan[m] = t;
   }
-  for (int m = 1; m <= SKINNY_GEMM_MAX_M; ++m)
+  for (int m = 1; m <= SKINNY_GEMM_MAX_M; ++m) {
     if (!h->plan[m].valid()) {
       fail(SKG_EINVAL, "no valid tactic for M = %d on this weight", m);
       skinny_gemm_destroy(h);
       return nullptr;
     }
+    if (ensure_workspace(h, h->plan[m]) != SKG_OK) {
+      const int code = g_last_status;
+      const std::string msg = g_err;
+      skinny_gemm_destroy(h);
+      fail(code, "%s", msg.c_str());
+      return nullptr;
+    }
+  }
   if (log_enabled()) {
     fprintf(stderr, "[skinny_gemm] prepared N=%lld K=%lld on %s (%d SMs):", static_cast<long long>(N),
             static_cast<long long>(K), di->name, di->sm_count);
@@ -646,6 +724,7 @@ int skinny_gemm_set_tactic(skinny_gemm_t h, int64_t M, const char* tactic) {
     return fail(SKG_EINVAL, "tactic %s does not fit: %s", tactic, why.c_str());
   if (active_clusters(h, t) <= 0)
     return fail(SKG_EINVAL, "tactic %s cannot be resident on this GPU", tactic);
+  if (ensure_workspace(h, t) != SKG_OK) return g_last_status;
   h->plan[M] = t;
   return ok();
 }
@@ -687,28 +766,59 @@ int skinny_gemm_autotune(skinny_gemm_t h, const int64_t* Ms, int nM, void* strea
     if (Ms[i] < 1 || Ms[i] > SKINNY_GEMM_MAX_M)
       return fail(SKG_EUNSUPPORTED_M, "M = %lld outside 1..%d", static_cast<long long>(Ms[i]),
                   SKINNY_GEMM_MAX_M);
-  const int reps = static_cast<int>(env_u64("SKINNY_GEMM_TUNE_REPS", 9));
-  const size_t flush_bytes = static_cast<size_t>(std::max(h->dev->l2_bytes, 1 << 20)) * 2;
-  void *flush = nullptr, *xbuf = nullptr, *obuf = nullptr;
+  e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+
+  // Steady-state timing, the way decode steps run: each candidate is captured
+  // as a CUDA graph of back-to-back launches (programmatic dependent launch
+  // between them) that rotate over R scratch copies of the weight's layout,
+  // R * weight bytes >= 2x L2, so every launch streams its weight from HBM.
+  // The copies' contents do not matter for timing; they are zero-filled.
+  const size_t wbytes = static_cast<size_t>(h->N) * h->ldw * 2;
+  const size_t l2 = static_cast<size_t>(std::max(h->dev->l2_bytes, 1 << 20));
+  const int R = static_cast<int>(std::min<size_t>(64, std::max<size_t>(2, (2 * l2 + wbytes - 1) / wbytes)));
+  const int L = R * std::max(1, (24 + R - 1) / R);  // launches per timed graph
+  const int reps = std::max(1, static_cast<int>(env_u64("SKINNY_GEMM_TUNE_REPS", 3)));
+  void *rot = nullptr, *xbuf = nullptr, *obuf = nullptr;
   cudaEvent_t e0 = nullptr, e1 = nullptr;
-  int rc = SKG_OK;
-  std::vector<float> times;
+  cudaStream_t ts = nullptr;
   auto cleanup = [&]() {
-    if (flush) cudaFree(flush);
+    if (ts) cudaStreamSynchronize(ts);
+    if (rot) cudaFree(rot);
     if (xbuf) cudaFree(xbuf);
     if (obuf) cudaFree(obuf);
     if (e0) cudaEventDestroy(e0);
     if (e1) cudaEventDestroy(e1);
+    if (ts) cudaStreamDestroy(ts);
   };
-  if ((e = cudaMalloc(&flush, flush_bytes)) != cudaSuccess ||
-      (e = cudaMalloc(&xbuf, static_cast<size_t>(SKINNY_GEMM_MAX_M) * h->K * 2)) != cudaSuccess ||
-      (e = cudaMalloc(&obuf, static_cast<size_t>(SKINNY_GEMM_MAX_M) * h->N * 4)) != cudaSuccess ||
-      (e = cudaMemsetAsync(flush, 0, flush_bytes, st)) != cudaSuccess ||
-      (e = cudaMemsetAsync(xbuf, 0, static_cast<size_t>(SKINNY_GEMM_MAX_M) * h->K * 2, st)) != cudaSuccess ||
+  const size_t xbytes = static_cast<size_t>(SKINNY_GEMM_MAX_M) * h->K * 2;
+  const size_t obytes = static_cast<size_t>(SKINNY_GEMM_MAX_M) * h->N * 4;
+  if ((e = cudaMalloc(&rot, wbytes * R)) != cudaSuccess ||
+      (e = cudaMalloc(&xbuf, xbytes)) != cudaSuccess ||
+      (e = cudaMalloc(&obuf, obytes)) != cudaSuccess ||
+      (e = cudaMemset(rot, 0, wbytes * R)) != cudaSuccess ||
+      (e = cudaMemset(xbuf, 0, xbytes)) != cudaSuccess ||
+      (e = cudaStreamCreateWithFlags(&ts, cudaStreamNonBlocking)) != cudaSuccess ||
       (e = cudaEventCreate(&e0)) != cudaSuccess || (e = cudaEventCreate(&e1)) != cudaSuccess) {
     cleanup();
     return cuda_fail(e, "autotune setup");
   }
+  std::vector<skinny_gemm_plan> shadow(R, *h);
+  for (int r = 0; r < R; ++r) {
+    skinny_gemm_plan& sh = shadow[r];
+    sh.W = static_cast<char*>(rot) + r * wbytes;
+    sh.debug_count = 0;
+    sh.x_stage = sh.out_stage = nullptr;
+    if (encode_map(&sh.wmap64, sh.W, h->N, h->K, h->ldw, 64, h->dtype,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B) != SKG_OK ||
+        encode_map(&sh.wmap128, sh.W, h->N, h->K, h->ldw, 128, h->dtype,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B) != SKG_OK) {
+      const int code = g_last_status;
+      cleanup();
+      return code;
+    }
+  }
+  int rc = SKG_OK;
   std::vector<int64_t> tuned;
   for (int i = 0; i < nM && rc == SKG_OK; ++i) {
     const int64_t M = Ms[i];
@@ -716,28 +826,57 @@ int skinny_gemm_autotune(skinny_gemm_t h, const int64_t* Ms, int nM, void* strea
     double best_us = 1e30;
     Tactic best;
     for (const Tactic& t : cand) {
-      times.clear();
-      rc = launch_tactic(h, t, xbuf, h->K, M, obuf, h->N, st);  // warm-up
-      for (int r = 0; r < reps && rc == SKG_OK; ++r) {
-        l2_flush_kernel<<<h->dev->sm_count * 4, 512, 0, st>>>(static_cast<const uint4*>(flush),
-                                                             flush_bytes / 16, nullptr);
-        cudaEventRecord(e0, st);
-        rc = launch_tactic(h, t, xbuf, h->K, M, obuf, h->N, st);
-        cudaEventRecord(e1, st);
-        if (rc != SKG_OK) break;
-        if ((e = cudaEventSynchronize(e1)) != cudaSuccess) {
-          rc = cuda_fail(e, "autotune timing");
-          break;
-        }
-        float ms = 0;
-        cudaEventElapsedTime(&ms, e0, e1);
-        times.push_back(ms);
-      }
+      rc = ensure_workspace(h, t);
       if (rc != SKG_OK) break;
-      std::sort(times.begin(), times.end());
-      const double us = 1000.0 * times[times.size() / 2];
+      for (skinny_gemm_plan& sh : shadow) {
+        sh.workspace = h->workspace;
+        sh.workspace_bytes = h->workspace_bytes;
+        sh.counters = h->counters;
+        sh.counters_bytes = h->counters_bytes;
+      }
+      cudaGraph_t graph = nullptr;
+      cudaGraphExec_t exec = nullptr;
+      e = cudaStreamBeginCapture(ts, cudaStreamCaptureModeThreadLocal);
+      if (e != cudaSuccess) {
+        rc = cuda_fail(e, "cudaStreamBeginCapture(autotune)");
+        break;
+      }
+      for (int l = 0; l < L && rc == SKG_OK; ++l)
+        rc = launch_tactic(&shadow[l % R], t, xbuf, h->K, M, obuf, h->N, ts);
+      e = cudaStreamEndCapture(ts, &graph);
+      if (rc != SKG_OK || e != cudaSuccess) {
+        if (graph) cudaGraphDestroy(graph);
+        if (rc == SKG_OK) rc = cuda_fail(e, "cudaStreamEndCapture(autotune)");
+        break;
+      }
+      e = cudaGraphInstantiate(&exec, graph, 0);
+      if (e != cudaSuccess) {
+        cudaGraphDestroy(graph);
+        rc = cuda_fail(e, "cudaGraphInstantiate(autotune)");
+        break;
+      }
+      float best_ms = 1e30f;
+      e = cudaGraphLaunch(exec, ts);  // warm-up
+      for (int r = 0; r < reps && e == cudaSuccess; ++r) {
+        cudaEventRecord(e0, ts);
+        e = cudaGraphLaunch(exec, ts);
+        cudaEventRecord(e1, ts);
+        if (e == cudaSuccess) e = cudaEventSynchronize(e1);
+        float ms = 0;
+        if (e == cudaSuccess) {
+          cudaEventElapsedTime(&ms, e0, e1);
+          best_ms = std::min(best_ms, ms);
+        }
+      }
+      cudaGraphExecDestroy(exec);
+      cudaGraphDestroy(graph);
+      if (e != cudaSuccess) {
+        rc = cuda_fail(e, "autotune timing");
+        break;
+      }
+      const double us = 1000.0 * best_ms / L;
       if (log_enabled())
-        fprintf(stderr, "[skinny_gemm] tune N=%lld K=%lld M=%lld %s %.2f us\n",
+        fprintf(stderr, "[skinny_gemm] tune N=%lld K=%lld M=%lld %s %.3f us\n",
                 static_cast<long long>(h->N), static_cast<long long>(h->K),
                 static_cast<long long>(M), tactic_str(t).c_str(), us);
       if (us < best_us) {
@@ -751,10 +890,8 @@ int skinny_gemm_autotune(skinny_gemm_t h, const int64_t* Ms, int nM, void* strea
       append_tactic_file(h, M, best, best_us);
     }
   }
-  e = cudaStreamSynchronize(st);
   cleanup();
   if (rc != SKG_OK) return rc;
-  if (e != cudaSuccess) return cuda_fail(e, "autotune sync");
   // Untuned M take the tuned tactic of the smallest tuned M' >= M.
   std::sort(tuned.begin(), tuned.end());
   for (int m = 1; m <= SKINNY_GEMM_MAX_M; ++m) {
@@ -777,6 +914,8 @@ int skinny_gemm_check_status(skinny_gemm_t h, void* stream) {
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(status)");
   if (v != 0) {
     cudaMemset(h->status, 0, sizeof v);
+    // a kernel that gave up may have left split-tile counters mid-count
+    if (h->counters) cudaMemset(h->counters, 0, h->counters_bytes);
     return fail(SKG_ETIMEOUT, "device watchdog: bounded wait expired (code 0x%08x)", v);
   }
   return ok();
@@ -793,6 +932,8 @@ int skinny_gemm_debug_inject_timeout(skinny_gemm_t h, int count, uint64_t timeou
 void skinny_gemm_destroy(skinny_gemm_t h) {
   if (h == nullptr) return;
   if (h->status) cudaFree(h->status);
+  if (h->workspace) cudaFree(h->workspace);
+  if (h->counters) cudaFree(h->counters);
   if (h->x_stage) cudaFree(h->x_stage);
   if (h->out_stage) cudaFree(h->out_stage);
   delete h;

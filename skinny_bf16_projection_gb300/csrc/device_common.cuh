@@ -31,6 +31,27 @@ __device__ __forceinline__ void report_status(uint32_t* status, uint32_t code) {
   if (status != nullptr) atomicCAS(status, 0u, code);
 }
 
+// Barrier among `nthreads` threads (whole warps) of the CTA, separate from __syncthreads.
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// L2-coherent load (bypasses L1), issued in program order so a run of them is in flight together.
+__device__ __forceinline__ float ld_cg_f32(const float* ptr) {
+  float v;
+  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(ptr) : "memory");
+  return v;
+}
+
+// Release this CTA's prior writes (ordered before by a CTA barrier), count one
+// arrival on *ctr at GPU scope, acquire the other arrivals' writes.
+__device__ __forceinline__ uint32_t arrive_count_acq_rel(uint32_t* ctr) {
+  uint32_t prev;
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(prev) : "l"(ctr) : "memory");
+  return prev;
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

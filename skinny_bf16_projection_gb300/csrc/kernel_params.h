@@ -31,6 +31,9 @@ struct KParams {
   uint64_t timeout_ns;    // bound of every spin wait
   int32_t debug_wait;     // nonzero: watchdog self-test, wait on a dead barrier and return
   int32_t pad_;
+  // stream-K kernel only: fp32 partial sums of split tiles and per-tile arrival counters
+  float* workspace;       // [gridDim.x][2][TOK][128]
+  uint32_t* counters;     // [ceil(N / 128)], zero between launches
 };
 
 // Shared-memory footprint of one configuration (bytes, including 1 KB of
@@ -46,7 +49,7 @@ __host__ __device__ constexpr uint32_t smem_bytes(int rows, int tok, int nbox, i
          static_cast<uint32_t>((2 * stages + 4) * 8) + 16;
 }
 
-enum Variant : int { kVariantMma = 1, kVariantTc = 2 };
+enum Variant : int { kVariantMma = 1, kVariantTc = 2, kVariantSk = 3 };
 
 struct KernelEntry {
   int variant;    // kVariantMma (mma.sync) or kVariantTc (tcgen05 / TMEM)
@@ -59,8 +62,15 @@ struct KernelEntry {
   const void* func;
 };
 
-// Defined in kernels_mma.cu and kernels_tc.cu.
+// Defined in kernels_mma.cu, kernels_tc.cu and kernels_sk.cu.
 const KernelEntry* mma_kernel_table(int* count);
 const KernelEntry* tc_kernel_table(int* count);
+const KernelEntry* sk_kernel_table(int* count);
+
+// Stream-K shared memory: stages plus barriers (no cluster receive buffer).
+__host__ __device__ constexpr uint32_t sk_smem_bytes(int tok, int nbox, int stages) {
+  return kSmemAlign + stages * stage_bytes(128, tok, nbox) +
+         static_cast<uint32_t>((2 * stages + 6) * 8) + 16;
+}
 
 }  // namespace skg

@@ -106,6 +106,10 @@ __global__ void __launch_bounds__(160) skinny_mma_kernel(const __grid_constant__
           tma_load_2d_hint(st + b * kWBox, &wmap, (kb0 + it * NBOX + b) * kBoxK, n0, full_bar(it),
                            policy);
       }
+      // Let the next kernel on the stream launch now: its CTAs can prefetch their
+      // own weight tiles while this grid streams (they still wait for our
+      // completion in griddepcontrol.wait before touching x or out).
+      pdl_launch_dependents();
       pdl_wait();
       for (int it = 0; it < pro; ++it) {
         const int nbi = min(NBOX, nb - it * NBOX);
@@ -128,7 +132,6 @@ __global__ void __launch_bounds__(160) skinny_mma_kernel(const __grid_constant__
           tma_load_2d(st + NBOX * kWBox + b * kXBox, &xmap, (kb0 + it * NBOX + b) * kBoxK, 0,
                       full_bar(s));
       }
-      pdl_launch_dependents();
     }
     __syncwarp();
   } else {

@@ -311,3 +311,22 @@ def test_autotune_refuses_during_capture():
     g.replay()
     torch.cuda.synchronize()
     assert torch.count_nonzero(y) == 0
+
+
+@pytest.mark.parametrize("N", [3584, 6288])
+def test_stream_k_every_tactic_full_size(N):
+    """Every stream-K candidate (1 or 2 CTAs per SM, every box/stage count) at the
+    full decode shapes: split tiles are finished by the last-arriving CTA."""
+    w, x, ref, s = full_case(N, 7168)
+    xd = x.to(DEV)
+    for odt in (torch.bfloat16, torch.float32):
+        proj = skg().Projection(w.to(DEV), odt, use_tactic_file=False)
+        for M in (1, 8, 32, 64):
+            sk = [t for t in proj.tactics(M) if t.startswith("sk:")]
+            assert sk, f"no stream-K candidate at M={M}"
+            for t in sk:
+                proj.set_tactic(M, t)
+                for _ in range(2):  # twice: the tile counters must be back at zero
+                    y = run_proj(proj, xd[:M], odt)
+                    assert_parity(y, ref[:M], s[:M], f"N={N} M={M} {odt} {t}")
+        proj.check_status()
