@@ -143,7 +143,7 @@ int skinny_gemm_run_overlap(skinny_gemm_t h_main, skinny_gemm_t h_fa, skinny_gem
  * smallest listed M' >= M, else keep the default (low_latency_gemm page,
  * autotune_kda_qkvg: autotune before CUDA graph capture).  Each candidate is
  * timed as a CUDA graph of back-to-back launches that rotate over scratch
- * copies of the weight's layout (>= 2x the L2 size, so reads come from HBM),
+ * copies of the weight's layout (>= 4.5x the L2 size, so reads come from HBM),
  * i.e. in the steady state of a decode step.  Synchronizes `stream`;
  * allocates and frees those copies; may grow the handle's workspace; writes
  * nothing the caller owns.  Must not be called while capturing (ECAPTURING).

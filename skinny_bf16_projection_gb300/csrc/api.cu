@@ -101,8 +101,10 @@ int encode_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, in
 }
 
 // ------------------------------------------------------------------ kernels / tactics
+// cl: cluster size (tc, mma); for stream-K, CTAs per SM (mode 0, "g") or
+// parts per row tile (mode 1, "p").
 struct Tactic {
-  int variant = 0, rows = 0, tok = 0, nbox = 0, stages = 0, cl = 0;
+  int variant = 0, rows = 0, tok = 0, nbox = 0, stages = 0, cl = 0, mode = 0;
   bool valid() const { return variant != 0; }
 };
 
@@ -110,8 +112,9 @@ struct Tactic {
 std::string tactic_str(const Tactic& t) {
   char b[96];
   const char* kind = t.variant == kVariantTc ? "tc" : (t.variant == kVariantSk ? "sk" : "mma");
-  snprintf(b, sizeof b, "%s:r%d:t%d:b%d:s%d:%c%d", kind, t.rows, t.tok, t.nbox, t.stages,
-           t.variant == kVariantSk ? 'g' : 'c', t.cl);
+  const char last = t.variant != kVariantSk ? 'c' : (t.mode == 1 ? 'p' : 'g');
+  snprintf(b, sizeof b, "%s:r%d:t%d:b%d:s%d:%c%d", kind, t.rows, t.tok, t.nbox, t.stages, last,
+           t.cl);
   return b;
 }
 
@@ -126,9 +129,10 @@ bool tactic_parse(const char* s, Tactic* t) {
     x.variant = kVariantTc;
   else if (strcmp(kind, "mma") == 0 && last == 'c')
     x.variant = kVariantMma;
-  else if (strcmp(kind, "sk") == 0 && last == 'g')
+  else if (strcmp(kind, "sk") == 0 && (last == 'g' || last == 'p')) {
     x.variant = kVariantSk;
-  else
+    x.mode = last == 'p' ? 1 : 0;
+  } else
     return false;
   *t = x;
   return true;
@@ -160,6 +164,7 @@ std::vector<const KernelEntry*> all_kernels() {
 
 struct DeviceInfo {
   int sm_count = 0, smem_optin = 0, l2_bytes = 0, major = 0, minor = 0;
+  int smem_per_sm = 0, smem_reserved = 0, regs_per_sm = 0, threads_per_sm = 0;
   char name[256] = {0};
   bool attrs_set = false;
 };
@@ -178,6 +183,10 @@ int device_info(int dev, DeviceInfo** out) {
     d.sm_count = prop.multiProcessorCount;
     d.smem_optin = static_cast<int>(prop.sharedMemPerBlockOptin);
     d.l2_bytes = prop.l2CacheSize;
+    d.smem_per_sm = static_cast<int>(prop.sharedMemPerMultiprocessor);
+    d.smem_reserved = static_cast<int>(prop.reservedSharedMemPerBlock);
+    d.regs_per_sm = prop.regsPerMultiprocessor;
+    d.threads_per_sm = prop.maxThreadsPerMultiProcessor;
     d.major = prop.major;
     d.minor = prop.minor;
     snprintf(d.name, sizeof d.name, "%s", prop.name);
@@ -189,6 +198,10 @@ int device_info(int dev, DeviceInfo** out) {
       if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic smem)");
       e = cudaFuncSetAttribute(k->func, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
       if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(non-portable cluster)");
+      // Operands arrive through TMA into shared memory; L1 is barely used.
+      e = cudaFuncSetAttribute(k->func, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(carveout)");
     }
     d.attrs_set = true;
   }
@@ -246,7 +259,9 @@ uint32_t tactic_smem(const Tactic& t) {
 int tactic_grid(const skinny_gemm_plan* h, const Tactic& t) {
   if (t.variant != kVariantSk) return ntiles_of(h, t) * t.cl;
   const int64_t units = static_cast<int64_t>(ntiles_of(h, t)) * h->kboxes;
-  return static_cast<int>(std::min<int64_t>(static_cast<int64_t>(t.cl) * h->dev->sm_count, units));
+  const int64_t want = t.mode == 1 ? static_cast<int64_t>(ntiles_of(h, t)) * t.cl
+                                   : static_cast<int64_t>(t.cl) * h->dev->sm_count;
+  return static_cast<int>(std::min<int64_t>(want, units));
 }
 int tactic_cluster(const Tactic& t) { return t.variant == kVariantSk ? 1 : t.cl; }
 // Stream-K scratch: two fp32 [TOK][128] partial-sum slots per CTA, one counter per tile.
@@ -270,7 +285,9 @@ bool tactic_fits(const skinny_gemm_plan* h, const Tactic& t, int64_t M, std::str
   if (k == nullptr) return no("no compiled kernel for this rows/tok/box/dtype combination");
   if (M > t.tok) return no("token tile smaller than M");
   if (t.variant == kVariantSk) {
-    if (t.cl != 1 && t.cl != 2) return no("stream-K runs 1 or 2 CTAs per SM");
+    if (t.mode == 0 && t.cl != 1 && t.cl != 2) return no("stream-K runs 1 or 2 CTAs per SM");
+    if (t.mode == 1 && (t.cl < 1 || t.cl > 64 || t.cl > h->kboxes))
+      return no("parts per tile must be 1..64 and at most the number of 64-wide K blocks");
   } else {
     bool pow2 = false;
     for (int c : kClusters) pow2 |= (c == t.cl);
@@ -349,15 +366,23 @@ int launch_tactic(skinny_gemm_plan* h, const Tactic& t, const void* x, int64_t l
   cfg.blockDim = dim3(static_cast<unsigned>(k->threads), 1, 1);
   cfg.dynamicSmemBytes = tactic_smem(t);
   cfg.stream = st;
+  // A cluster attribute, even of size 1, makes the launch a cluster launch,
+  // which was measured to allow only one cluster per SM: attach it only for
+  // real clusters.
   cudaLaunchAttribute attrs[2];
-  attrs[0].id = cudaLaunchAttributeClusterDimension;
-  attrs[0].val.clusterDim.x = static_cast<unsigned>(tactic_cluster(t));
-  attrs[0].val.clusterDim.y = 1;
-  attrs[0].val.clusterDim.z = 1;
-  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attrs[1].val.programmaticStreamSerializationAllowed = 1;
+  int na = 0;
+  attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
+  if (tactic_cluster(t) > 1) {
+    attrs[na].id = cudaLaunchAttributeClusterDimension;
+    attrs[na].val.clusterDim.x = static_cast<unsigned>(tactic_cluster(t));
+    attrs[na].val.clusterDim.y = 1;
+    attrs[na].val.clusterDim.z = 1;
+    ++na;
+  }
   cfg.attrs = attrs;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = static_cast<unsigned>(na);
   const CUtensorMap* wmap = t.rows == 64 ? &h->wmap64 : &h->wmap128;
   void* args[3] = {const_cast<CUtensorMap*>(wmap), &xmap, &p};
   cudaError_t e = cudaLaunchKernelExC(&cfg, k->func, args);
@@ -366,9 +391,30 @@ int launch_tactic(skinny_gemm_plan* h, const Tactic& t, const void* x, int64_t l
 }
 
 // Clusters of this tactic that fit on the GPU at once (0: cannot launch).
+// Without clusters this is resident CTAs per SM x SMs.
 int active_clusters(const skinny_gemm_plan* h, const Tactic& t) {
   const KernelEntry* k = find_kernel(t, h->dtype, h->out_dtype);
   if (k == nullptr) return 0;
+  if (tactic_cluster(t) == 1) {
+    // Counted here rather than by cudaOccupancyMaxActiveBlocksPerMultiprocessor,
+    // which answers one block per SM for any kernel that allocates tensor
+    // memory (measured: four such blocks of 32 columns ran at once per SM).
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, k->func) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return 0;
+    }
+    const DeviceInfo& d = *h->dev;
+    const int regs = ((fa.numRegs + 7) / 8) * 8 * k->threads;
+    int per_sm = std::min(32, d.threads_per_sm / k->threads);
+    per_sm = std::min(per_sm, regs > 0 ? d.regs_per_sm / regs : per_sm);
+    per_sm = std::min(per_sm, d.smem_per_sm / static_cast<int>(tactic_smem(t) + d.smem_reserved));
+    const int tmem_cols = t.variant == kVariantSk  ? (2 * t.tok <= 32 ? 32 : (2 * t.tok <= 64 ? 64 : 128))
+                          : t.variant == kVariantTc ? (t.tok <= 32 ? 32 : 64)
+                                                    : 0;
+    if (tmem_cols > 0) per_sm = std::min(per_sm, 512 / tmem_cols);
+    return std::max(per_sm, 0) * d.sm_count;
+  }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(tactic_grid(h, t)), 1, 1);
   cfg.blockDim = dim3(static_cast<unsigned>(k->threads), 1, 1);
@@ -405,13 +451,26 @@ std::vector<Tactic> candidates(const skinny_gemm_plan* h, int64_t M) {
       if (k->variant != variant || k->tok != tok || k->in_dtype != h->dtype ||
           k->out_dtype != h->out_dtype)
         continue;
-      for (int cl : kClusters)
+      std::vector<std::pair<int, int>> grids;  // (cl, mode)
+      if (variant == kVariantSk) {
+        for (int g : {1, 2}) grids.push_back({g, 0});
+        for (int pp : {1, 2, 3, 4, 6, 8, 12, 16}) grids.push_back({pp, 1});
+      } else {
+        for (int cl : kClusters) grids.push_back({cl, 0});
+      }
+      for (const auto& gm : grids)
         for (int s = 2; s <= 8; ++s) {
-          Tactic t{variant, k->rows, tok, k->nbox, s, cl};
+          Tactic t{variant, k->rows, tok, k->nbox, s, gm.first, gm.second};
           if (!tactic_fits(h, t, M, nullptr)) continue;
-          if (active_clusters(h, t) <= 0) continue;
+          const int act = active_clusters(h, t);
           // stream-K: every CTA of the grid must be resident at once (one wave)
-          if (variant == kVariantSk && active_clusters(h, t) < tactic_grid(h, t)) continue;
+          if (act <= 0 || (variant == kVariantSk && act < tactic_grid(h, t))) {
+            if (log_enabled())
+              fprintf(stderr, "[skinny_gemm] candidate %s rejected: %d resident of %d (smem %u)\n",
+                      tactic_str(t).c_str(), act * tactic_cluster(t), tactic_grid(h, t),
+                      tactic_smem(t));
+            continue;
+          }
           out.push_back(t);
         }
     }
@@ -419,39 +478,46 @@ std::vector<Tactic> candidates(const skinny_gemm_plan* h, int64_t M) {
   return out;
 }
 
-// Default (untuned) choice: tcgen05 kernel, the smallest token tile >= M,
-// two 64-wide boxes per stage, the cluster split that first gives at least
-// one CTA per SM, and as many stages as fit two CTAs per SM (one when the
-// grid is smaller than the GPU).
+// Default (untuned) choice, from what the autotuner picked on GB300 for the
+// 3584x7168 and 6288x7168 weights with every weight read from HBM:
+//   M <= 8   mma.sync, 128-row tiles, 8-token tile, 2 boxes x 3 stages
+//   M <= 16  mma.sync, 64-row tiles, 16-token tile, 2 boxes x 2 stages
+//   M <= 32  tcgen05, 32-token tile, 2 boxes x 2 stages
+//   M <= 64  tcgen05, 64-token tile, 1 box x 3 stages
+// with the cluster split (split-K factor) that gives about 1.4 CTAs per SM,
+// at most 8; fewer stages where shared memory or the K range is short.  Any
+// choice that does not fit falls back to fewer stages, then to the tcgen05
+// kernel with the same rule.
 Tactic default_tactic(const skinny_gemm_plan* h, int64_t M) {
   Tactic best;
-  int tok = 0;
-  for (int tk : kTcToks)
-    if (tk >= M) {
-      tok = tk;
-      break;
+  auto with_cluster = [&](Tactic t) {
+    const int ntiles = static_cast<int>((h->N + t.rows - 1) / t.rows);
+    int cl = 1;
+    while (cl < 8 && ntiles * cl * 10 < h->dev->sm_count * 14 && cl * 2 <= h->kboxes &&
+           t.rows % (cl * 2) == 0)
+      cl *= 2;
+    t.cl = cl;
+    const int iters = ((h->kboxes + cl - 1) / cl + t.nbox - 1) / t.nbox;
+    t.stages = std::max(1, std::min(t.stages, iters));
+    for (; t.stages >= 1; --t.stages)
+      if (tactic_fits(h, t, M, nullptr)) return t;
+    return Tactic{};
+  };
+  Tactic t;
+  if (M <= 8)
+    t = with_cluster(Tactic{kVariantMma, 128, 8, 2, 3, 1, 0});
+  else if (M <= 16)
+    t = with_cluster(Tactic{kVariantMma, 64, 16, 2, 2, 1, 0});
+  else if (M <= 32)
+    t = with_cluster(Tactic{kVariantTc, 128, 32, 2, 2, 1, 0});
+  else
+    t = with_cluster(Tactic{kVariantTc, 128, 64, 1, 3, 1, 0});
+  if (t.valid()) return t;
+  for (int tok : kTcToks)
+    if (tok >= M) {
+      t = with_cluster(Tactic{kVariantTc, 128, tok, 1, 2, 1, 0});
+      if (t.valid()) return t;
     }
-  if (tok == 0) return best;
-  const int rows = 128;
-  const int ntiles = static_cast<int>((h->N + rows - 1) / rows);
-  int cl = 1;
-  while (cl < 8 && ntiles * cl < h->dev->sm_count && cl * 2 <= h->kboxes) cl *= 2;
-  const int ctas = ntiles * cl;
-  const int per_sm = ctas > h->dev->sm_count ? 2 : 1;
-  const int budget = h->dev->smem_optin / per_sm - 2048;
-  const int nbox = 2;
-  const int per_cta_boxes = (h->kboxes + cl - 1) / cl;
-  const int max_iters = (per_cta_boxes + nbox - 1) / nbox;
-  int stages = 2;
-  while (stages < 8 && stages < max_iters &&
-         static_cast<int>(smem_bytes(rows, tok, nbox, stages + 1)) <= budget)
-    ++stages;
-  Tactic t{kVariantTc, rows, tok, nbox, stages, cl};
-  if (tactic_fits(h, t, M, nullptr)) return t;
-  for (int s = stages; s >= 1; --s) {
-    t.stages = s;
-    if (tactic_fits(h, t, M, nullptr)) return t;
-  }
   return best;
 }
 
@@ -772,11 +838,12 @@ int skinny_gemm_autotune(skinny_gemm_t h, const int64_t* Ms, int nM, void* strea
   // Steady-state timing, the way decode steps run: each candidate is captured
   // as a CUDA graph of back-to-back launches (programmatic dependent launch
   // between them) that rotate over R scratch copies of the weight's layout,
-  // R * weight bytes >= 2x L2, so every launch streams its weight from HBM.
+  // R * weight bytes >= 4.5x L2, so every launch streams its weight from HBM.
   // The copies' contents do not matter for timing; they are zero-filled.
   const size_t wbytes = static_cast<size_t>(h->N) * h->ldw * 2;
   const size_t l2 = static_cast<size_t>(std::max(h->dev->l2_bytes, 1 << 20));
-  const int R = static_cast<int>(std::min<size_t>(64, std::max<size_t>(2, (2 * l2 + wbytes - 1) / wbytes)));
+  // >= 4.5x L2: a cyclic read of only ~2x L2 was measured still partly L2-fed.
+  const int R = static_cast<int>(std::min<size_t>(64, std::max<size_t>(2, (9 * l2 / 2 + wbytes - 1) / wbytes)));
   const int L = R * std::max(1, (24 + R - 1) / R);  // launches per timed graph
   const int reps = std::max(1, static_cast<int>(env_u64("SKINNY_GEMM_TUNE_REPS", 3)));
   void *rot = nullptr, *xbuf = nullptr, *obuf = nullptr;

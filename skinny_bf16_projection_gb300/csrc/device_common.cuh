@@ -43,6 +43,15 @@ __device__ __forceinline__ float ld_cg_f32(const float* ptr) {
   return v;
 }
 
+__device__ __forceinline__ float4 ld_cg_f32x4(const float* ptr) {
+  float4 v;
+  asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(ptr)
+               : "memory");
+  return v;
+}
+
 // Release this CTA's prior writes (ordered before by a CTA barrier), count one
 // arrival on *ctr at GPU scope, acquire the other arrivals' writes.
 __device__ __forceinline__ uint32_t arrive_count_acq_rel(uint32_t* ctr) {

@@ -279,29 +279,61 @@ __global__ void __launch_bounds__(192) skinny_sk_kernel(const __grid_constant__ 
       }
       named_barrier_sync(1, 128);
       if (*flag_g != 0u) {
-        // Sum every part in CTA order (the same order whichever CTA arrives last).
-        float sum[TOK];
+        // Sum every part in CTA order (the same order whichever CTA arrives
+        // last).  Work items are (token, 4 consecutive rows); a thread keeps
+        // kIB items x kPB parts of loads in flight, then adds them in part
+        // order, so each batch costs one L2 round trip.
+        constexpr int kPB = 8;
+        constexpr int kIB = 4;
+        const int parts = c_last - c_first + 1;
+        const int items = M * (ROWS / 4);
+        for (int i0 = static_cast<int>(ep_tid); i0 < items; i0 += 128 * kIB) {
+          float4 acc[kIB];
 #pragma unroll
-        for (int tk = 0; tk < TOK; ++tk) sum[tk] = 0.0f;
-        for (int cq = c_first; cq <= c_last; ++cq) {
-          if (cq == c) {
+          for (int ii = 0; ii < kIB; ++ii) acc[ii] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          for (int q0 = 0; q0 < parts; q0 += kPB) {
+            const float* base_q[kPB];
 #pragma unroll
-            for (int tk = 0; tk < TOK; ++tk) sum[tk] += v[tk];
-            continue;
+            for (int q = 0; q < kPB; ++q) {
+              const int cq = c_first + min(q0 + q, parts - 1);
+              const int first_q = static_cast<int>(static_cast<int64_t>(cq) * U / G) / kb;
+              const int slot = cq * 2 + (t == first_q ? 0 : 1);
+              base_q[q] = p.workspace + static_cast<int64_t>(slot) * TOK * ROWS;
+            }
+            float4 pv[kIB][kPB];
+#pragma unroll
+            for (int ii = 0; ii < kIB; ++ii) {
+              const int item = i0 + ii * 128;
+              const int off = (item / (ROWS / 4)) * ROWS + (item % (ROWS / 4)) * 4;
+#pragma unroll
+              for (int q = 0; q < kPB; ++q) {
+                pv[ii][q] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                if (item < items && q0 + q < parts) pv[ii][q] = ld_cg_f32x4(base_q[q] + off);
+              }
+            }
+#pragma unroll
+            for (int ii = 0; ii < kIB; ++ii)
+#pragma unroll
+              for (int q = 0; q < kPB; ++q)
+                if (q0 + q < parts) {
+                  acc[ii].x += pv[ii][q].x;
+                  acc[ii].y += pv[ii][q].y;
+                  acc[ii].z += pv[ii][q].z;
+                  acc[ii].w += pv[ii][q].w;
+                }
           }
-          const int first_q = static_cast<int>(static_cast<int64_t>(cq) * U / G) / kb;
-          const int slot = cq * 2 + (t == first_q ? 0 : 1);
-          const float* ws = p.workspace + static_cast<int64_t>(slot) * TOK * ROWS + row;
-          float part[TOK];
 #pragma unroll
-          for (int tk = 0; tk < TOK; ++tk) part[tk] = tk < M ? ld_cg_f32(ws + tk * ROWS) : 0.0f;
-#pragma unroll
-          for (int tk = 0; tk < TOK; ++tk) sum[tk] += part[tk];
-        }
-        if (n < p.N) {
-#pragma unroll
-          for (int tk = 0; tk < TOK; ++tk)
-            if (tk < M) out[static_cast<int64_t>(tk) * p.ldo + n] = to_out<OutT>(sum[tk]);
+          for (int ii = 0; ii < kIB; ++ii) {
+            const int item = i0 + ii * 128;
+            if (item >= items) continue;
+            const int tk = item / (ROWS / 4);
+            const int nb0 = t * ROWS + (item % (ROWS / 4)) * 4;
+            OutT* const o = out + static_cast<int64_t>(tk) * p.ldo + nb0;
+            if (nb0 + 0 < p.N) o[0] = to_out<OutT>(acc[ii].x);
+            if (nb0 + 1 < p.N) o[1] = to_out<OutT>(acc[ii].y);
+            if (nb0 + 2 < p.N) o[2] = to_out<OutT>(acc[ii].z);
+            if (nb0 + 3 < p.N) o[3] = to_out<OutT>(acc[ii].w);
+          }
         }
         if (ep_tid == 0) p.counters[t] = 0u;  // ready for the next launch
       }
