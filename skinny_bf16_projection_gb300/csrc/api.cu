@@ -251,8 +251,9 @@ int ntiles_of(const skinny_gemm_plan* h, const Tactic& t) {
   return static_cast<int>((h->N + t.rows - 1) / t.rows);
 }
 uint32_t tactic_smem(const Tactic& t) {
-  return t.variant == kVariantSk ? sk_smem_bytes(t.tok, t.nbox, t.stages)
-                                 : smem_bytes(t.rows, t.tok, t.nbox, t.stages);
+  if (t.variant == kVariantSk) return sk_smem_bytes(t.tok, t.nbox, t.stages);
+  if (t.variant == kVariantTc) return tc_smem_bytes(t.tok, t.nbox, t.stages);
+  return smem_bytes(t.rows, t.tok, t.nbox, t.stages);
 }
 // CTAs launched: row tiles x cluster size, or (stream-K) CTAs-per-SM x SMs,
 // capped at the number of work units.

@@ -191,6 +191,17 @@ __device__ __forceinline__ void st_async_b32(uint32_t remote_addr, float v, uint
                : "memory");
 }
 
+// Remote 16-byte store (four fp32) counted on the remote CTA's mbarrier.
+__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float a, float b, float c,
+                                            float d, uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::
+          "r"(remote_addr),
+      "r"(__float_as_uint(a)), "r"(__float_as_uint(b)), "r"(__float_as_uint(c)),
+      "r"(__float_as_uint(d)), "r"(remote_bar)
+      : "memory");
+}
+
 // ---------------------------------------------------------------- output
 template <typename T>
 __device__ __forceinline__ T to_out(float v);

@@ -67,6 +67,17 @@ const KernelEntry* mma_kernel_table(int* count);
 const KernelEntry* tc_kernel_table(int* count);
 const KernelEntry* sk_kernel_table(int* count);
 
+// tcgen05 cluster kernel: the receive buffer is [cluster][rows/cluster][TOK + 4]
+// fp32 (token-contiguous rows, padded so 16-byte reads of consecutive rows
+// fall in different banks).
+__host__ __device__ constexpr uint32_t tc_red_bytes(int tok) {
+  return static_cast<uint32_t>(128 * (tok + 4) * 4);
+}
+__host__ __device__ constexpr uint32_t tc_smem_bytes(int tok, int nbox, int stages) {
+  return kSmemAlign + stages * stage_bytes(128, tok, nbox) + tc_red_bytes(tok) +
+         static_cast<uint32_t>((2 * stages + 4) * 8) + 16;
+}
+
 // Stream-K shared memory: stages plus barriers (no cluster receive buffer).
 __host__ __device__ constexpr uint32_t sk_smem_bytes(int tok, int nbox, int stages) {
   return kSmemAlign + stages * stage_bytes(128, tok, nbox) +

@@ -48,8 +48,7 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
   uint8_t* const gbase = smem_raw + (base - raw);
   const int S = p.stages;
   const uint32_t red = base + static_cast<uint32_t>(S) * kStage;
-  float* const red_g = reinterpret_cast<float*>(gbase + static_cast<uint32_t>(S) * kStage);
-  const uint32_t bars = red + red_bytes(ROWS, TOK);
+  const uint32_t bars = red + tc_red_bytes(TOK);
   const uint32_t done_bar = bars + 8u * (2 * S);
   const uint32_t recv_bar = done_bar + 8u;
   const uint32_t dbg_bar = done_bar + 16u;
@@ -90,7 +89,7 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
     }
     mbar_init(done_bar, 1);
     mbar_init(recv_bar, 1);
-    if (csize > 1) mbar_arrive_expect_tx(recv_bar, (csize - 1) * RS * M * 4u);
+    if (csize > 1) mbar_arrive_expect_tx(recv_bar, (csize - 1) * RS * ((M + 3) / 4) * 16u);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -197,30 +196,56 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
     }
   } else {
     cluster_wait_acquire();  // every peer's receive barrier is initialised
+    // Receive buffer [rank][RS][TP]: each row's tokens contiguous (16-byte pushes),
+    // rows padded by 4 floats so the reduce's 16-byte reads do not collide.
+    constexpr int TP = TOK + 4;
+    const int MG = (M + 3) / 4;  // groups of 4 tokens carried
     const uint32_t owner = static_cast<uint32_t>(r / RS);
     const int rs = r % RS;
+    const uint32_t row_off = ((rank * RS + rs) * TP) * 4u;
     if (owner == rank) {
 #pragma unroll
-      for (int t = 0; t < TOK; ++t)
-        if (t < M) red_g[(rank * TOK + t) * RS + rs] = v[t];
+      for (int g = 0; g < TOK / 4; ++g)
+        if (g < MG)
+          asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(red + row_off + g * 16u),
+                       "f"(v[4 * g]), "f"(v[4 * g + 1]), "f"(v[4 * g + 2]), "f"(v[4 * g + 3])
+                       : "memory");
     } else {
-      const uint32_t raddr = mapa_shared(red + ((rank * TOK) * RS + rs) * 4u, owner);
+      const uint32_t raddr = mapa_shared(red + row_off, owner);
       const uint32_t rbar = mapa_shared(recv_bar, owner);
 #pragma unroll
-      for (int t = 0; t < TOK; ++t)
-        if (t < M) st_async_b32(raddr + static_cast<uint32_t>(t * RS * 4), v[t], rbar);
+      for (int g = 0; g < TOK / 4; ++g)
+        if (g < MG)
+          st_async_v4(raddr + static_cast<uint32_t>(g * 16), v[4 * g], v[4 * g + 1], v[4 * g + 2],
+                      v[4 * g + 3], rbar);
     }
     __syncthreads();
     if (!mbar_wait_bounded<true>(recv_bar, 0, p.timeout_ns))
       report_status(p.status, kStatusTimeoutRecv);
     const int nbase = n0 + static_cast<int>(rank) * RS;
-    for (int idx = threadIdx.x; idx < RS * M; idx += blockDim.x) {
+    for (int idx = threadIdx.x; idx < RS * MG; idx += blockDim.x) {
       const int rs2 = idx % RS;
-      const int t = idx / RS;
-      float acc = 0.0f;
-      for (uint32_t k = 0; k < csize; ++k) acc += red_g[(k * TOK + t) * RS + rs2];
+      const int g = idx / RS;
+      float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      for (uint32_t k = 0; k < csize; ++k) {
+        float4 q;
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(q.x), "=f"(q.y), "=f"(q.z), "=f"(q.w)
+                     : "r"(red + ((k * RS + rs2) * TP + 4 * g) * 4u)
+                     : "memory");
+        acc.x += q.x;
+        acc.y += q.y;
+        acc.z += q.z;
+        acc.w += q.w;
+      }
       const int n = nbase + rs2;
-      if (n < p.N) out[static_cast<int64_t>(t) * p.ldo + n] = to_out<OutT>(acc);
+      if (n < p.N) {
+        OutT* const o = out + static_cast<int64_t>(4 * g) * p.ldo + n;
+        o[0] = to_out<OutT>(acc.x);
+        if (4 * g + 1 < M) o[p.ldo] = to_out<OutT>(acc.y);
+        if (4 * g + 2 < M) o[2 * p.ldo] = to_out<OutT>(acc.z);
+        if (4 * g + 3 < M) o[3 * p.ldo] = to_out<OutT>(acc.w);
+      }
     }
   }
 
