@@ -244,6 +244,104 @@ def reference_arm(args, rank, world):
     return 0
 
 
+# ----------------------------------------------------------------------------- other workloads
+def graph_time_us(torch, stream, dev, fn, n_launch: int, reps: int = 5) -> float:
+    """Per-call time of fn(i) for i in range(n_launch), captured as one CUDA graph and
+    replayed (best of reps), in microseconds per call."""
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.graph(g, stream=side):
+        for i in range(n_launch):
+            fn(i)
+    stream.wait_stream(side)
+    g.replay()
+    torch.cuda.synchronize()
+    best = float("inf")
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        best = min(best, a.elapsed_time(b) * 1e3 / n_launch)
+    return best
+
+
+def other_workloads(torch, skg, pin, dev, l2, peak_gbs):
+    """The other workloads, each projection reading its weight from HBM (rotated copies
+    >= 4.5x L2), autotuned, timed as CUDA-graph replays: the packed 6288x7168 weight at
+    M = 1..32, both weights at the larger token tiles with bf16 and fp32 output, and the
+    overlapped decode step (packed projection on the main stream, F_A -> F_B chain on an
+    aux stream)."""
+    stream = torch.cuda.current_stream(dev)
+    res = {}
+    for N in (3584, 6288):
+        K = 7168
+        wbytes = N * K * 2
+        R = max(2, math.ceil(4.5 * l2 / wbytes))
+        w, x = pin.case(N, K, seed=0)
+        ws = [w.to(dev)]
+        ws += [ws[0].clone() for _ in range(R - 1)]
+        Ms = (1, 2, 4, 8, 16, 32, 48, 64)
+        p16 = [skg.Projection(t) for t in ws]
+        p32 = [skg.Projection(t, torch.float32) for t in ws]
+        p16[0].autotune(list(Ms))
+        for M in Ms:
+            for p in p16[1:] + p32:
+                p.set_tactic(M, p16[0].plan(M))
+        xd = x.to(dev)
+        entry = {}
+        for M in Ms:
+            for odt, projs in ((torch.bfloat16, p16), (torch.float32, p32)):
+                if odt == torch.float32 and M < 4:
+                    continue
+                out = torch.empty((M, N), dtype=odt, device=dev)
+                xm = xd[:M].contiguous()
+                us = graph_time_us(torch, stream, dev, lambda i: projs[i % R].run(xm, out),
+                                   R * max(1, math.ceil(48 / R)))
+                gbs = wbytes / us / 1e3
+                entry[f"M{M}_{'bf16' if odt == torch.bfloat16 else 'fp32'}"] = {
+                    "us": round(us, 3), "weight_GBps": round(gbs, 1),
+                    "frac": round(gbs / peak_gbs, 4), "tactic": projs[0].plan(M)}
+        res[f"W[{N},{K}] rotated x{R}"] = entry
+        if N == 6288:
+            # overlapped step: main = packed projection, aux = F_A (first 128 packed rows) -> F_B
+            wfb = pin.weight(1536, 128, seed=1).to(dev)
+            fa = [skg.Projection(t[:128]) for t in ws]
+            fb = skg.Projection(wfb)
+            aux = torch.cuda.Stream(dev, priority=-1)
+            ev = (torch.cuda.Event(), torch.cuda.Event())
+            step = {}
+            for chain in (1, 4):
+                for M in (1, 4, 8, 16, 32):
+                    xm = xd[:M].contiguous()
+                    om = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+                    fo = torch.empty((M, 128), dtype=torch.bfloat16, device=dev)
+                    fbo = torch.empty((chain, M, 1536), dtype=torch.bfloat16, device=dev)
+                    skg.run_overlap(p16[0], fa[0], fb, xm, om, fo, fbo, chain=chain,
+                                    aux_stream=aux, events=ev)  # creates the events
+                    torch.cuda.synchronize()
+                    us = graph_time_us(
+                        torch, stream, dev,
+                        lambda i: skg.run_overlap(p16[i % R], fa[i % R], fb, xm, om, fo, fbo,
+                                                  chain=chain, aux_stream=aux, events=ev),
+                        R * max(1, math.ceil(24 / R)))
+                    alg = wbytes + 1536 * 128 * 2 * chain
+                    step[f"chain{chain}_M{M}"] = {"step_us": round(us, 3),
+                                                  "weight_GBps": round(alg / us / 1e3, 1),
+                                                  "frac": round(alg / us / 1e3 / peak_gbs, 4)}
+            res["overlap step: W[6288,7168] main || F_A[128,7168] -> F_B[1536,128] aux"] = step
+            for p in fa:
+                p.close()
+            fb.close()
+        for p in p16 + p32:
+            p.close()
+        del ws
+        torch.cuda.empty_cache()
+    return res
+
+
 # ----------------------------------------------------------------------------- our arm
 def main():
     ap = argparse.ArgumentParser()
@@ -254,6 +352,8 @@ def main():
     ap.add_argument("--no-tune", action="store_true", help="use the default plan")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip the per-config table (6288x7168, token tiles 48/64, fp32, overlap)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank, world, local = dist_setup()
@@ -407,6 +507,8 @@ def main():
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks,
     }
+    if not args.no_other_workloads:
+        line["other_workloads"] = other_workloads(torch, skg, pin, dev, l2, peaks["hbm_gbs"])
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         gbs, cores, sample, _ = oracle_step_rate(args.cpu_seconds)
         line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores,
