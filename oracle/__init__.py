@@ -69,6 +69,10 @@ def _load():
                                               ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                               p_f64, p_f64, ctypes.c_int]
             lib.oracle_projection.restype = None
+            lib.oracle_projection_typed.argtypes = lib.oracle_projection.argtypes + [ctypes.c_int]
+            lib.oracle_projection_typed.restype = None
+            lib.oracle_fp16_to_f64.argtypes = [p_u16, ctypes.c_int64, p_f64]
+            lib.oracle_fp16_to_f64.restype = None
             lib.oracle_bf16_to_f64.argtypes = [p_u16, ctypes.c_int64, p_f64]
             lib.oracle_bf16_to_f64.restype = None
             lib.oracle_round_bf16.argtypes = [p_f64, ctypes.c_int64, p_u16]
@@ -80,28 +84,41 @@ def _load():
 
 
 def _as_bits(a) -> np.ndarray:
-    """Accept a numpy uint16 array or a CPU torch bf16 tensor; return uint16 bits."""
+    """Accept a numpy uint16 array or a CPU torch bf16/fp16 tensor; return uint16 bits."""
     if isinstance(a, np.ndarray):
         if a.dtype != np.uint16:
-            raise TypeError("oracle inputs are bf16 bit patterns (uint16)")
+            raise TypeError("oracle inputs are 16-bit patterns (uint16)")
         return a
     import torch  # only for accepting torch CPU tensors as input containers
-    if not isinstance(a, torch.Tensor) or a.dtype != torch.bfloat16:
-        raise TypeError("oracle inputs are bf16 tensors or uint16 bit arrays")
+    if not isinstance(a, torch.Tensor) or a.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError("oracle inputs are bf16/fp16 tensors or uint16 bit arrays")
     t = a.detach().cpu()
     return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _input_type(x, w, dtype):
+    """0 for bf16, 1 for fp16: explicit `dtype`, else the torch tensors' type."""
+    if dtype is not None:
+        return {"bf16": 0, "fp16": 1}[dtype]
+    import torch
+    kinds = {a.dtype for a in (x, w) if isinstance(a, torch.Tensor)}
+    if len(kinds) > 1:
+        raise TypeError("x and w must have the same 16-bit type")
+    return 1 if kinds == {torch.float16} else 0
 
 
 def max_threads() -> int:
     return int(_load().oracle_max_threads())
 
 
-def projection(x, w, *, with_scale: bool = True, threads: int = 0):
+def projection(x, w, *, with_scale: bool = True, threads: int = 0, dtype: str | None = None):
     """ref[M, N] = x[M, K] @ w[N, K]^T in fp64 (and s[M, N] for the bound).
 
-    x, w: 2-D bf16 (uint16 bits or torch bf16, any row pitch with unit inner
-    stride).  Returns (ref, s) as float64 arrays (s is None without scale).
+    x, w: 2-D bf16 or fp16 (torch tensors, or uint16 bit arrays with dtype="bf16"
+    or "fp16"; any row pitch with unit inner stride).  Returns (ref, s) as
+    float64 arrays (s is None without scale).
     """
+    kind = _input_type(x, w, dtype)
     xb, wb = _as_bits(x), _as_bits(w)
     if xb.ndim != 2 or wb.ndim != 2 or xb.shape[1] != wb.shape[1]:
         raise ValueError(f"shapes x{xb.shape} w{wb.shape}: need x[M,K], w[N,K]")
@@ -114,11 +131,11 @@ def projection(x, w, *, with_scale: bool = True, threads: int = 0):
     lib = _load()
     p_u16 = ctypes.POINTER(ctypes.c_uint16)
     p_f64 = ctypes.POINTER(ctypes.c_double)
-    lib.oracle_projection(
+    lib.oracle_projection_typed(
         xb.ctypes.data_as(p_u16), xb.strides[0] // 2,
         wb.ctypes.data_as(p_u16), wb.strides[0] // 2,
         M, N, K, ref.ctypes.data_as(p_f64),
-        s.ctypes.data_as(p_f64) if s is not None else None, int(threads))
+        s.ctypes.data_as(p_f64) if s is not None else None, int(threads), kind)
     return ref, s
 
 
@@ -127,6 +144,15 @@ def bf16_to_f64(bits) -> np.ndarray:
     b = np.ascontiguousarray(_as_bits(bits))
     out = np.empty(b.shape, dtype=np.float64)
     _load().oracle_bf16_to_f64(b.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16)), b.size,
+                               out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))
+    return out
+
+
+def fp16_to_f64(bits) -> np.ndarray:
+    """Exact widening of IEEE binary16 bit patterns to float64."""
+    b = np.ascontiguousarray(_as_bits(bits))
+    out = np.empty(b.shape, dtype=np.float64)
+    _load().oracle_fp16_to_f64(b.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16)), b.size,
                                out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))
     return out
 

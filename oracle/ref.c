@@ -75,14 +75,38 @@ void oracle_round_bf16(const double* v, int64_t n, uint16_t* out) {
     for (int64_t i = 0; i < n; ++i) out[i] = double_to_bf16_bits(v[i]);
 }
 
+/* IEEE binary16 bit pattern -> exact double: sign, 5-bit exponent (bias 15),
+ * 10-bit fraction; exponent 0 holds zero and subnormals (fraction * 2^-24),
+ * exponent 31 holds infinities and NaNs. */
+static double fp16_bits_to_double(uint16_t bits) {
+    const int sign = bits >> 15;
+    const int e = (bits >> 10) & 0x1F;
+    const int f = bits & 0x3FF;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + f), e - 25);
+    return sign ? -v : v;
+}
+
+void oracle_fp16_to_f64(const uint16_t* bits, int64_t n, double* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = fp16_bits_to_double(bits[i]);
+}
+
 /*
- * out[M, N] = x[M, K] @ W[N, K]^T in double.  x has row pitch ldx elements,
- * W row pitch ldw elements; ref and s are dense [M, N].  s may be NULL.
- * nthreads <= 0 means "OpenMP default"; without OpenMP the loop is serial.
+ * out[M, N] = x[M, K] @ W[N, K]^T in double, for 16-bit inputs of the given
+ * type (0 = bf16, 1 = fp16; both operands the same type).  x has row pitch
+ * ldx elements, W row pitch ldw elements; ref and s are dense [M, N].  s may
+ * be NULL.  nthreads <= 0 means "OpenMP default"; without OpenMP the loop is
+ * serial.
  */
-void oracle_projection(const uint16_t* x, int64_t ldx, const uint16_t* w, int64_t ldw,
-                       int64_t M, int64_t N, int64_t K, double* ref, double* s,
-                       int nthreads) {
+void oracle_projection_typed(const uint16_t* x, int64_t ldx, const uint16_t* w, int64_t ldw,
+                             int64_t M, int64_t N, int64_t K, double* ref, double* s,
+                             int nthreads, int dtype) {
+    double (*widen)(uint16_t) = dtype == 1 ? fp16_bits_to_double : bf16_bits_to_double;
 #ifdef _OPENMP
     if (nthreads > 0) omp_set_num_threads(nthreads);
 #pragma omp parallel for schedule(static)
@@ -93,7 +117,7 @@ void oracle_projection(const uint16_t* x, int64_t ldx, const uint16_t* w, int64_
             const uint16_t* xm = x + m * ldx;
             double acc = 0.0, sq = 0.0;
             for (int64_t k = 0; k < K; ++k) {
-                double p = bf16_bits_to_double(xm[k]) * bf16_bits_to_double(wn[k]);
+                double p = widen(xm[k]) * widen(wn[k]);
                 acc += p;
                 sq += p * p;
             }
@@ -101,6 +125,13 @@ void oracle_projection(const uint16_t* x, int64_t ldx, const uint16_t* w, int64_
             if (s) s[m * N + n] = sqrt(sq);
         }
     }
+}
+
+/* The bf16 projection (the operation's own input type). */
+void oracle_projection(const uint16_t* x, int64_t ldx, const uint16_t* w, int64_t ldw,
+                       int64_t M, int64_t N, int64_t K, double* ref, double* s,
+                       int nthreads) {
+    oracle_projection_typed(x, ldx, w, ldw, M, N, K, ref, s, nthreads, 0);
 }
 
 int oracle_max_threads(void) {

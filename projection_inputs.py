@@ -24,19 +24,22 @@ def weight(N: int, K: int, seed: int = 0, std: float | None = None) -> torch.Ten
     return (torch.randn(N, K, generator=g, dtype=torch.float32) * std).to(torch.bfloat16)
 
 
-def case(N: int, K: int, seed: int = 0, std: float | None = None, max_tokens: int = MAX_TOKENS):
-    """(W[N, K], x_full[max_tokens, K]) drawn in that order from one generator."""
+def case(N: int, K: int, seed: int = 0, std: float | None = None, max_tokens: int = MAX_TOKENS,
+         dtype: torch.dtype = torch.bfloat16):
+    """(W[N, K], x_full[max_tokens, K]) drawn in that order from one generator,
+    rounded to `dtype` (bf16 or fp16)."""
     g = torch.Generator().manual_seed(seed)
     std = 1.0 / math.sqrt(K) if std is None else std
-    w = (torch.randn(N, K, generator=g, dtype=torch.float32) * std).to(torch.bfloat16)
-    x = torch.randn(max_tokens, K, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    w = (torch.randn(N, K, generator=g, dtype=torch.float32) * std).to(dtype)
+    x = torch.randn(max_tokens, K, generator=g, dtype=torch.float32).to(dtype)
     return w, x
 
 
-def small_integers(rows: int, cols: int, seed: int, lo: int = -8, hi: int = 8) -> torch.Tensor:
-    """Integers in [lo, hi] as bf16 (exactly representable)."""
+def small_integers(rows: int, cols: int, seed: int, lo: int = -8, hi: int = 8,
+                   dtype: torch.dtype = torch.bfloat16) -> torch.Tensor:
+    """Integers in [lo, hi] as bf16 or fp16 (exactly representable)."""
     g = torch.Generator().manual_seed(seed)
-    return torch.randint(lo, hi + 1, (rows, cols), generator=g).to(torch.bfloat16)
+    return torch.randint(lo, hi + 1, (rows, cols), generator=g).to(dtype)
 
 
 def one_hot_rows(M: int, K: int, cols) -> torch.Tensor:

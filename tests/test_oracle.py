@@ -262,3 +262,59 @@ def test_pins_catch_planted_mistakes(tmp_path, name):
     want = (xi.double().numpy().astype(np.int64) @ wi.double().numpy().astype(np.int64).T)
     caught.append(not np.array_equal(run(xi, wi), want.astype(np.float64)))
     assert any(caught), f"mutation {name} slipped past every pin"
+
+
+# ---------------------------------------------------------------- fp16 inputs
+def test_fp16_widening_all_bit_patterns_match_numpy():
+    """Every binary16 pattern widens exactly as numpy's float16 -> float64 does."""
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = oracle.fp16_to_f64(pats)
+    want = pats.view(np.float16).astype(np.float64)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
+
+
+@pytest.mark.parametrize("pattern,value", [
+    (0x3C00, 1.0), (0xC000, -2.0), (0x0001, 2.0 ** -24), (0x0400, 2.0 ** -14),
+    (0x7BFF, 65504.0), (0x3555, 0.333251953125), (0x3C01, 1.0 + 2.0 ** -10),
+])
+def test_fp16_widening_known_values(pattern, value):
+    assert oracle.fp16_to_f64(np.array([pattern], dtype=np.uint16))[0] == value
+
+
+def test_fp16_one_hot_and_small_integers():
+    N, K = 33, 40
+    w = pin.weight(N, K, seed=8).to(torch.float16)
+    x = pin.one_hot_rows(3, K, [0, 17, 39]).to(torch.float16)
+    ref, s = oracle.projection(x, w)
+    wv = w.double().numpy()
+    for m, j in enumerate([0, 17, 39]):
+        assert np.array_equal(ref[m], wv[:, j]) and np.array_equal(s[m], np.abs(wv[:, j]))
+    xi = pin.small_integers(5, 700, seed=3, dtype=torch.float16)
+    wi = pin.small_integers(9, 700, seed=4, dtype=torch.float16)
+    ref, _ = oracle.projection(xi, wi)
+    want = xi.numpy().astype(np.int64) @ wi.numpy().astype(np.int64).T
+    assert np.array_equal(ref, want.astype(np.float64))
+
+
+def test_fp16_brute_force_exact_rationals():
+    g = torch.Generator().manual_seed(12)
+    x = (torch.randn(3, 6, generator=g) * 5).to(torch.float16)
+    w = (torch.randn(4, 6, generator=g) * 0.2).to(torch.float16)
+    ref, _ = oracle.projection(x, w)
+    ex, _ = _exact(x.double().numpy(), w.double().numpy())
+    xa, wa = x.double().abs().numpy(), w.double().abs().numpy()
+    for m in range(3):
+        for n in range(4):
+            bound = 1.01 * 5 * EPS64 * float(np.dot(xa[m], wa[n]))
+            assert abs(Fraction(ref[m, n]) - ex[m][n]) <= Fraction(bound)
+
+
+def test_bit_arrays_need_an_explicit_type():
+    b = np.zeros((2, 8), dtype=np.uint16)
+    r0, _ = oracle.projection(b, b, dtype="fp16")
+    assert np.all(r0 == 0)
+    with pytest.raises(TypeError):
+        oracle.projection(torch.zeros(2, 8, dtype=torch.float16), torch.zeros(2, 8, dtype=torch.bfloat16))
