@@ -305,6 +305,28 @@ def other_workloads(torch, skg, pin, dev, l2, peak_gbs):
                     "us": round(us, 3), "weight_GBps": round(gbs, 1),
                     "frac": round(gbs / peak_gbs, 4), "tactic": projs[0].plan(M)}
         res[f"W[{N},{K}] rotated x{R}"] = entry
+        if N == 3584:
+            # FP16 operands (both x and W), fp16 output, same rotation
+            w16 = [t.to(torch.float16) for t in ws]
+            q16 = [skg.Projection(t, torch.float16) for t in w16]
+            q16[0].autotune([1, 8, 32])
+            for M in (1, 8, 32):
+                for q in q16[1:]:
+                    q.set_tactic(M, q16[0].plan(M))
+            x16 = x.to(torch.float16).to(dev)
+            e16 = {}
+            for M in (1, 8, 32):
+                out = torch.empty((M, N), dtype=torch.float16, device=dev)
+                xm = x16[:M].contiguous()
+                us = graph_time_us(torch, stream, dev, lambda i: q16[i % R].run(xm, out),
+                                   R * max(1, math.ceil(48 / R)))
+                gbs = wbytes / us / 1e3
+                e16[f"M{M}_fp16"] = {"us": round(us, 3), "weight_GBps": round(gbs, 1),
+                                     "frac": round(gbs / peak_gbs, 4), "tactic": q16[0].plan(M)}
+            res[f"W[{N},{K}] fp16 operands rotated x{R}"] = e16
+            for q in q16:
+                q.close()
+            del w16
         if N == 6288:
             # overlapped step: main = packed projection, aux = F_A (first 128 packed rows) -> F_B
             wfb = pin.weight(1536, 128, seed=1).to(dev)

@@ -9,7 +9,8 @@
  * @ weight[N, K]^T, x and out packed row-major, 32 B aligned); page
  * "vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.gemm.projection",
  * class PreparedProjection (prepare once, then run(x, out) into a
- * caller-owned out; BF16 or FP32 output).
+ * caller-owned out; BF16 or FP32 output).  FP16 operands are also accepted
+ * (same projection page: "BF16/FP16 [N, K]" weights), with FP16 or FP32 output.
  *
  * Conventions for every entry point:
  *   - Pointers named W, x, out, fa, out_* are DEVICE pointers on the current
@@ -39,9 +40,9 @@ extern "C" {
 
 typedef struct skinny_gemm_plan* skinny_gemm_t; /* opaque prepared projection */
 
-/* Element types.  W and x: SKG_BF16 (or SKG_FP16, both operands the same).
- * out: SKG_BF16 or SKG_FP32 (projection page, PreparedProjection: "BF16/FP16
- * [N, K]" weights, output dtype BF16 or FP32). */
+/* Element types.  W and x: SKG_BF16 or SKG_FP16 (both operands the same type).
+ * out: SKG_FP32 or the operands' own type (projection page, PreparedProjection:
+ * "BF16/FP16 [N, K]" weights, output dtype BF16 or FP32). */
 enum skinny_gemm_dtype { SKG_BF16 = 0, SKG_FP16 = 1, SKG_FP32 = 2 };
 
 /* Return codes.  The pages raise ValueError for the EINVAL/EALIGN cases
@@ -73,7 +74,8 @@ enum skinny_gemm_status {
  *
  * W is BORROWED: the handle stores its address; W must stay allocated and
  * must not move while the handle lives (its contents may change between
- * runs).  Requirements: N >= 1, K >= 8, K % 8 == 0, W 16-byte aligned.
+ * runs).  Requirements: N >= 1, K >= 8, K % 8 == 0, W 16-byte aligned;
+ * dtype SKG_BF16 or SKG_FP16; out_dtype SKG_FP32 or equal to dtype.
  * Allocates a small device status word (the watchdog).  Must not be called
  * while a stream on this device is capturing (returns NULL, ECAPTURING).
  * Returns NULL on error (see skinny_gemm_last_error / skinny_gemm_last_status).

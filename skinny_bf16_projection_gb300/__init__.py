@@ -16,7 +16,8 @@ from ._native import MAX_M, SkinnyGemmError
 
 __all__ = ["Projection", "run_overlap", "SkinnyGemmError", "MAX_M", "library_path"]
 
-_OUT_CODES = {torch.bfloat16: _native.SKG_BF16, torch.float32: _native.SKG_FP32}
+_OUT_CODES = {torch.bfloat16: _native.SKG_BF16, torch.float16: _native.SKG_FP16,
+              torch.float32: _native.SKG_FP32}
 _IN_CODES = {torch.bfloat16: _native.SKG_BF16, torch.float16: _native.SKG_FP16}
 
 
@@ -42,13 +43,15 @@ def _matrix(t: torch.Tensor, name: str) -> tuple[int, int]:
 class Projection:
     """A prepared projection ``out = x @ weight.T`` for 1..64 tokens.
 
-    ``weight`` [N, K] (bf16, CUDA, unit inner stride) is borrowed: this object
-    keeps a reference so it stays alive, and it must not be moved or resized.
-    ``out_dtype`` is torch.bfloat16 or torch.float32.
+    ``weight`` [N, K] (bf16 or fp16, CUDA, unit inner stride) is borrowed: this
+    object keeps a reference so it stays alive, and it must not be moved or
+    resized.  ``out_dtype`` is torch.float32 or the weight's own dtype (default).
     """
 
-    def __init__(self, weight: torch.Tensor, out_dtype: torch.dtype = torch.bfloat16, *,
+    def __init__(self, weight: torch.Tensor, out_dtype: torch.dtype | None = None, *,
                  use_tactic_file: bool = True):
+        if out_dtype is None:
+            out_dtype = weight.dtype
         if not weight.is_cuda:
             raise ValueError("weight must be a CUDA tensor")
         if weight.dtype not in _IN_CODES:

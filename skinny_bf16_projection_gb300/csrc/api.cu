@@ -600,10 +600,13 @@ skinny_gemm_t skinny_gemm_prepare_ex(const void* W, int64_t N, int64_t K, int64_
                                      int out_dtype, unsigned flags) {
   g_last_status = 0;
   if (W == nullptr) return fail(SKG_EINVAL, "null weight pointer"), nullptr;
-  if (dtype != SKG_BF16)
-    return fail(SKG_EINVAL, "weight dtype %d unsupported: BF16 only", dtype), nullptr;
-  if (out_dtype != SKG_BF16 && out_dtype != SKG_FP32)
-    return fail(SKG_EINVAL, "unsupported projection output dtype %d (BF16 or FP32)", out_dtype),
+  if (dtype != SKG_BF16 && dtype != SKG_FP16)
+    return fail(SKG_EINVAL, "weight dtype %d unsupported: BF16 or FP16", dtype), nullptr;
+  // Output: FP32, or the operands' own 16-bit type.
+  if (out_dtype != SKG_FP32 && out_dtype != dtype)
+    return fail(SKG_EINVAL,
+                "unsupported projection output dtype %d for %s operands (%s or FP32)", out_dtype,
+                dtype == SKG_FP16 ? "FP16" : "BF16", dtype == SKG_FP16 ? "FP16" : "BF16"),
            nullptr;
   if (N < 1 || K < 8 || N > (1ll << 31) - 1 || K > (1ll << 31) - 1)
     return fail(SKG_EINVAL, "weight shape [%lld, %lld] out of range", static_cast<long long>(N),

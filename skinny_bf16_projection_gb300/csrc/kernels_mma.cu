@@ -246,19 +246,27 @@ __global__ void __launch_bounds__(160) skinny_mma_kernel(const __grid_constant__
   }
 }
 
-#define SKG_MMA_ENTRY(MT, TOK, NBOX, OUTT, OUTCODE)                                          \
+#define SKG_MMA_ENTRY(MT, TOK, NBOX, OUTT, OUTCODE, FP16)                                   \
   KernelEntry {                                                                              \
-    kVariantMma, 64 * MT, TOK, NBOX, 0, OUTCODE, 160,                                        \
-        reinterpret_cast<const void*>(&skinny_mma_kernel<MT, TOK, NBOX, OUTT, false>)        \
+    kVariantMma, 64 * MT, TOK, NBOX, FP16 ? 1 : 0, OUTCODE, 160,                             \
+        reinterpret_cast<const void*>(&skinny_mma_kernel<MT, TOK, NBOX, OUTT, FP16>)         \
   }
 
 #define SKG_MMA_ROW(MT, OUTT, OUTCODE)                                                       \
-  SKG_MMA_ENTRY(MT, 8, 2, OUTT, OUTCODE), SKG_MMA_ENTRY(MT, 8, 4, OUTT, OUTCODE),            \
-      SKG_MMA_ENTRY(MT, 16, 2, OUTT, OUTCODE), SKG_MMA_ENTRY(MT, 16, 4, OUTT, OUTCODE),      \
-      SKG_MMA_ENTRY(MT, 32, 2, OUTT, OUTCODE), SKG_MMA_ENTRY(MT, 32, 4, OUTT, OUTCODE)
+  SKG_MMA_ENTRY(MT, 8, 2, OUTT, OUTCODE, false), SKG_MMA_ENTRY(MT, 8, 4, OUTT, OUTCODE, false),  \
+      SKG_MMA_ENTRY(MT, 16, 2, OUTT, OUTCODE, false),                                        \
+      SKG_MMA_ENTRY(MT, 16, 4, OUTT, OUTCODE, false),                                        \
+      SKG_MMA_ENTRY(MT, 32, 2, OUTT, OUTCODE, false), SKG_MMA_ENTRY(MT, 32, 4, OUTT, OUTCODE, false)
 
-static const KernelEntry kMmaTable[] = {SKG_MMA_ROW(1, __nv_bfloat16, 0), SKG_MMA_ROW(2, __nv_bfloat16, 0),
-                                        SKG_MMA_ROW(1, float, 2), SKG_MMA_ROW(2, float, 2)};
+// fp16 operands (both x and W): two 64-wide boxes per stage only.
+#define SKG_MMA_ROW16(MT, OUTT, OUTCODE)                                                     \
+  SKG_MMA_ENTRY(MT, 8, 2, OUTT, OUTCODE, true), SKG_MMA_ENTRY(MT, 16, 2, OUTT, OUTCODE, true), \
+      SKG_MMA_ENTRY(MT, 32, 2, OUTT, OUTCODE, true)
+
+static const KernelEntry kMmaTable[] = {
+    SKG_MMA_ROW(1, __nv_bfloat16, 0), SKG_MMA_ROW(2, __nv_bfloat16, 0), SKG_MMA_ROW(1, float, 2),
+    SKG_MMA_ROW(2, float, 2),         SKG_MMA_ROW16(1, __half, 1),      SKG_MMA_ROW16(2, __half, 1),
+    SKG_MMA_ROW16(1, float, 2),       SKG_MMA_ROW16(2, float, 2)};
 
 const KernelEntry* mma_kernel_table(int* count) {
   *count = static_cast<int>(sizeof(kMmaTable) / sizeof(kMmaTable[0]));

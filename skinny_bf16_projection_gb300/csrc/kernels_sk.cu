@@ -73,7 +73,7 @@ __device__ __forceinline__ int cta_of_unit(int64_t u, int64_t U, int64_t G) {
 
 }  // namespace
 
-template <int TOK, int NBOX, typename OutT>
+template <int TOK, int NBOX, typename OutT, bool kFp16>
 __global__ void __launch_bounds__(192) skinny_sk_kernel(const __grid_constant__ CUtensorMap wmap,
                                                       const __grid_constant__ CUtensorMap xmap,
                                                       const KParams p) {
@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(192) skinny_sk_kernel(const __grid_constant__ 
   constexpr uint32_t kXBox = TOK * kBoxRowBytes;
   constexpr uint32_t kStage = stage_bytes(ROWS, TOK, NBOX);
   constexpr uint32_t kTmemCols = 2 * TOK <= 32 ? 32u : (2 * TOK <= 64 ? 64u : 128u);
-  constexpr uint32_t kIdesc = mma_idesc<false>(ROWS, TOK);
+  constexpr uint32_t kIdesc = mma_idesc<kFp16>(ROWS, TOK);
   static_assert(TOK % 16 == 0 && TOK >= 16 && TOK <= 64, "M=128 MMA needs N % 16 == 0");
 
   extern __shared__ uint8_t smem_raw[];
@@ -354,20 +354,25 @@ __global__ void __launch_bounds__(192) skinny_sk_kernel(const __grid_constant__ 
   }
 }
 
-#define SKG_SK_ENTRY(TOK, NBOX, OUTT, OUTCODE)                                          \
+#define SKG_SK_ENTRY(TOK, NBOX, OUTT, OUTCODE, FP16)                                    \
   KernelEntry {                                                                         \
-    kVariantSk, 128, TOK, NBOX, 0, OUTCODE, 192,                                        \
-        reinterpret_cast<const void*>(&skinny_sk_kernel<TOK, NBOX, OUTT>)               \
+    kVariantSk, 128, TOK, NBOX, FP16 ? 1 : 0, OUTCODE, 192,                             \
+        reinterpret_cast<const void*>(&skinny_sk_kernel<TOK, NBOX, OUTT, FP16>)         \
   }
 
 #define SKG_SK_ROW(OUTT, OUTCODE)                                                       \
-  SKG_SK_ENTRY(16, 1, OUTT, OUTCODE), SKG_SK_ENTRY(16, 2, OUTT, OUTCODE),               \
-      SKG_SK_ENTRY(16, 4, OUTT, OUTCODE), SKG_SK_ENTRY(32, 1, OUTT, OUTCODE),           \
-      SKG_SK_ENTRY(32, 2, OUTT, OUTCODE), SKG_SK_ENTRY(32, 4, OUTT, OUTCODE),           \
-      SKG_SK_ENTRY(64, 1, OUTT, OUTCODE), SKG_SK_ENTRY(64, 2, OUTT, OUTCODE),           \
-      SKG_SK_ENTRY(64, 4, OUTT, OUTCODE)
+  SKG_SK_ENTRY(16, 1, OUTT, OUTCODE, false), SKG_SK_ENTRY(16, 2, OUTT, OUTCODE, false), \
+      SKG_SK_ENTRY(16, 4, OUTT, OUTCODE, false), SKG_SK_ENTRY(32, 1, OUTT, OUTCODE, false), \
+      SKG_SK_ENTRY(32, 2, OUTT, OUTCODE, false), SKG_SK_ENTRY(32, 4, OUTT, OUTCODE, false), \
+      SKG_SK_ENTRY(64, 1, OUTT, OUTCODE, false), SKG_SK_ENTRY(64, 2, OUTT, OUTCODE, false), \
+      SKG_SK_ENTRY(64, 4, OUTT, OUTCODE, false)
 
-static const KernelEntry kSkTable[] = {SKG_SK_ROW(__nv_bfloat16, 0), SKG_SK_ROW(float, 2)};
+#define SKG_SK_ROW16(OUTT, OUTCODE)                                                     \
+  SKG_SK_ENTRY(16, 2, OUTT, OUTCODE, true), SKG_SK_ENTRY(32, 2, OUTT, OUTCODE, true),   \
+      SKG_SK_ENTRY(64, 2, OUTT, OUTCODE, true)
+
+static const KernelEntry kSkTable[] = {SKG_SK_ROW(__nv_bfloat16, 0), SKG_SK_ROW(float, 2),
+                                       SKG_SK_ROW16(__half, 1), SKG_SK_ROW16(float, 2)};
 
 const KernelEntry* sk_kernel_table(int* count) {
   *count = static_cast<int>(sizeof(kSkTable) / sizeof(kSkTable[0]));

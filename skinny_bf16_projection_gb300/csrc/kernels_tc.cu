@@ -264,20 +264,27 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
   }
 }
 
-#define SKG_TC_ENTRY(TOK, NBOX, OUTT, OUTCODE)                                              \
+#define SKG_TC_ENTRY(TOK, NBOX, OUTT, OUTCODE, FP16)                                        \
   KernelEntry {                                                                             \
-    kVariantTc, 128, TOK, NBOX, 0, OUTCODE, 128,                                            \
-        reinterpret_cast<const void*>(&skinny_tc_kernel<TOK, NBOX, OUTT, false>)            \
+    kVariantTc, 128, TOK, NBOX, FP16 ? 1 : 0, OUTCODE, 128,                                 \
+        reinterpret_cast<const void*>(&skinny_tc_kernel<TOK, NBOX, OUTT, FP16>)             \
   }
 
 #define SKG_TC_ROW(OUTT, OUTCODE)                                                           \
-  SKG_TC_ENTRY(16, 1, OUTT, OUTCODE), SKG_TC_ENTRY(16, 2, OUTT, OUTCODE),                   \
-      SKG_TC_ENTRY(16, 4, OUTT, OUTCODE), SKG_TC_ENTRY(32, 1, OUTT, OUTCODE),               \
-      SKG_TC_ENTRY(32, 2, OUTT, OUTCODE), SKG_TC_ENTRY(32, 4, OUTT, OUTCODE),               \
-      SKG_TC_ENTRY(64, 1, OUTT, OUTCODE), SKG_TC_ENTRY(64, 2, OUTT, OUTCODE),               \
-      SKG_TC_ENTRY(64, 4, OUTT, OUTCODE)
+  SKG_TC_ENTRY(16, 1, OUTT, OUTCODE, false), SKG_TC_ENTRY(16, 2, OUTT, OUTCODE, false),     \
+      SKG_TC_ENTRY(16, 4, OUTT, OUTCODE, false), SKG_TC_ENTRY(32, 1, OUTT, OUTCODE, false), \
+      SKG_TC_ENTRY(32, 2, OUTT, OUTCODE, false), SKG_TC_ENTRY(32, 4, OUTT, OUTCODE, false), \
+      SKG_TC_ENTRY(64, 1, OUTT, OUTCODE, false), SKG_TC_ENTRY(64, 2, OUTT, OUTCODE, false), \
+      SKG_TC_ENTRY(64, 4, OUTT, OUTCODE, false)
 
-static const KernelEntry kTcTable[] = {SKG_TC_ROW(__nv_bfloat16, 0), SKG_TC_ROW(float, 2)};
+// fp16 operands: one or two boxes per stage.
+#define SKG_TC_ROW16(OUTT, OUTCODE)                                                         \
+  SKG_TC_ENTRY(16, 1, OUTT, OUTCODE, true), SKG_TC_ENTRY(16, 2, OUTT, OUTCODE, true),       \
+      SKG_TC_ENTRY(32, 1, OUTT, OUTCODE, true), SKG_TC_ENTRY(32, 2, OUTT, OUTCODE, true),   \
+      SKG_TC_ENTRY(64, 1, OUTT, OUTCODE, true), SKG_TC_ENTRY(64, 2, OUTT, OUTCODE, true)
+
+static const KernelEntry kTcTable[] = {SKG_TC_ROW(__nv_bfloat16, 0), SKG_TC_ROW(float, 2),
+                                       SKG_TC_ROW16(__half, 1), SKG_TC_ROW16(float, 2)};
 
 const KernelEntry* tc_kernel_table(int* count) {
   *count = static_cast<int>(sizeof(kTcTable) / sizeof(kTcTable[0]));
