@@ -306,6 +306,19 @@ def other_workloads(torch, skg, pin, dev, l2, peak_gbs):
                     "frac": round(gbs / peak_gbs, 4), "tactic": projs[0].plan(M)}
         res[f"W[{N},{K}] rotated x{R}"] = entry
         if N == 3584:
+            # fused residual epilogue, in place: out = x @ W^T + out
+            eres = {}
+            for M in (1, 8, 32):
+                out = torch.zeros((M, N), dtype=torch.bfloat16, device=dev)
+                xm = xd[:M].contiguous()
+                us = graph_time_us(torch, stream, dev,
+                                   lambda i: p16[i % R].run(xm, out, residual=out),
+                                   R * max(1, math.ceil(48 / R)))
+                gbs = wbytes / us / 1e3
+                eres[f"M{M}_bf16_residual"] = {"us": round(us, 3), "weight_GBps": round(gbs, 1),
+                                               "frac": round(gbs / peak_gbs, 4),
+                                               "tactic": p16[0].plan(M)}
+            res[f"W[{N},{K}] + residual (in place) rotated x{R}"] = eres
             # FP16 operands (both x and W), fp16 output, same rotation
             w16 = [t.to(torch.float16) for t in ws]
             q16 = [skg.Projection(t, torch.float16) for t in w16]

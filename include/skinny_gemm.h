@@ -110,6 +110,19 @@ int skinny_gemm_run_strided(skinny_gemm_t h, const void* x, int64_t ldx, int64_t
                             void* out, int64_t ldo, void* stream);
 
 /*
+ * out[M, N] = x[M, K] @ W^T + residual[M, N], fused: the residual (in the
+ * prepared output type, row pitch ldr >= N, aligned to its element size) is
+ * added to the fp32 sum before the one rounding to the output type (page
+ * "vllm.models.kimi_k3.nvidia.low_latency_gemm", try_low_latency_gemm(x,
+ * weight, residual) and select_kimi_k3_backend(..., has_residual)).
+ * residual may be out itself (same pointer and pitch: in place); any other
+ * overlap with out is rejected (EINVAL).  Otherwise as skinny_gemm_run_strided.
+ */
+int skinny_gemm_run_residual(skinny_gemm_t h, const void* x, int64_t ldx, int64_t M,
+                             const void* residual, int64_t ldr, void* out, int64_t ldo,
+                             void* stream);
+
+/*
  * End-to-end call with HOST buffers: copies x_host [M, K] (pinned host memory
  * gives an asynchronous copy) into a device staging buffer owned by the
  * handle, runs the projection, copies the result into out_host [M, N] and

@@ -139,6 +139,25 @@ def projection(x, w, *, with_scale: bool = True, threads: int = 0, dtype: str | 
     return ref, s
 
 
+def projection_residual(x, w, residual, *, threads: int = 0):
+    """(x @ w^T + residual, s): the projection with a residual added, in fp64.
+
+    The residual [M, N] (torch bf16 / fp16 / fp32, or float64 array) is widened
+    exactly and added to the fp64 sum once (page "vllm.models.kimi_k3.nvidia.
+    low_latency_gemm", try_low_latency_gemm(x, weight, residual)).  s is the
+    projection's own scale, unchanged by the residual.
+    """
+    ref, s = projection(x, w, threads=threads)
+    if isinstance(residual, np.ndarray):
+        r = residual.astype(np.float64)
+    else:
+        import torch
+        r = residual.detach().cpu().to(torch.float64).numpy()  # exact widening
+    if r.shape != ref.shape:
+        raise ValueError(f"residual {r.shape} vs output {ref.shape}")
+    return ref + r, s
+
+
 def bf16_to_f64(bits) -> np.ndarray:
     """Exact widening of bf16 bit patterns to float64."""
     b = np.ascontiguousarray(_as_bits(bits))

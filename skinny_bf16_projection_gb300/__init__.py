@@ -73,16 +73,25 @@ class Projection:
         self.device = weight.device
 
     # ---------------------------------------------------------------- running
-    def run(self, x: torch.Tensor, out: torch.Tensor, stream=None) -> torch.Tensor:
-        """Write x @ W^T into the caller's ``out`` (no allocation); returns out."""
+    def run(self, x: torch.Tensor, out: torch.Tensor, stream=None,
+            residual: torch.Tensor | None = None) -> torch.Tensor:
+        """Write x @ W^T (+ residual) into the caller's ``out`` (no allocation);
+        returns out.  ``residual`` has out's shape and dtype and may be out itself."""
         xp, ldx = _matrix(x, "x")
         op, ldo = _matrix(out, "out")
         if x.shape[1] != self.K or out.shape[1] != self.N or out.shape[0] != x.shape[0]:
             raise ValueError(f"shapes x{tuple(x.shape)} out{tuple(out.shape)} for W[{self.N}, {self.K}]")
         if x.dtype != self.weight.dtype or out.dtype != self.out_dtype:
             raise ValueError(f"dtypes x {x.dtype} / out {out.dtype}")
-        _native.check(self._lib.skinny_gemm_run_strided(
-            self._h, xp, ldx, x.shape[0], op, ldo, _stream_ptr(stream)))
+        if residual is None:
+            _native.check(self._lib.skinny_gemm_run_strided(
+                self._h, xp, ldx, x.shape[0], op, ldo, _stream_ptr(stream)))
+            return out
+        if residual.shape != out.shape or residual.dtype != out.dtype:
+            raise ValueError(f"residual {tuple(residual.shape)} {residual.dtype} vs out")
+        rp, ldr = _matrix(residual, "residual")
+        _native.check(self._lib.skinny_gemm_run_residual(
+            self._h, xp, ldx, x.shape[0], rp, ldr, op, ldo, _stream_ptr(stream)))
         return out
 
     def __call__(self, x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:

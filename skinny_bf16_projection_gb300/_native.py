@@ -27,6 +27,7 @@ SIGNATURES = [
     ("skinny_gemm_prepare_ex", _vp, [_vp, _i64, _i64, _i64, _int, _int, ctypes.c_uint]),
     ("skinny_gemm_run", _int, [_vp, _vp, _i64, _vp, _vp]),
     ("skinny_gemm_run_strided", _int, [_vp, _vp, _i64, _i64, _vp, _i64, _vp]),
+    ("skinny_gemm_run_residual", _int, [_vp, _vp, _i64, _i64, _vp, _i64, _vp, _i64, _vp]),
     ("skinny_gemm_run_host", _int, [_vp, _vp, _i64, _vp, _vp]),
     ("skinny_gemm_run_overlap", _int, [_vp, _vp, _vp, _int, _vp, _i64, _vp, _vp, _vp, _vp, _vp,
                                        _vp, _vp]),

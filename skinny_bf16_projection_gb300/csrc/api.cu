@@ -333,7 +333,8 @@ int ensure_workspace(skinny_gemm_plan* h, const Tactic& t) {
 }
 
 int launch_tactic(skinny_gemm_plan* h, const Tactic& t, const void* x, int64_t ldx, int64_t M,
-                  void* out, int64_t ldo, cudaStream_t st) {
+                  void* out, int64_t ldo, cudaStream_t st, const void* residual = nullptr,
+                  int64_t ldr = 0) {
   const KernelEntry* k = find_kernel(t, h->dtype, h->out_dtype);
   if (k == nullptr) return fail(SKG_EINVAL, "no kernel for tactic %s", tactic_str(t).c_str());
   if (t.variant == kVariantSk) {
@@ -357,6 +358,8 @@ int launch_tactic(skinny_gemm_plan* h, const Tactic& t, const void* x, int64_t l
   p.timeout_ns = h->timeout_ns;
   p.workspace = h->workspace;
   p.counters = h->counters;
+  p.residual = residual;
+  p.ldr = ldr;
   if (h->debug_count > 0) {
     --h->debug_count;
     p.debug_wait = 1;
@@ -699,6 +702,28 @@ int skinny_gemm_run_strided(skinny_gemm_t h, const void* x, int64_t ldx, int64_t
   int rc = validate_run(h, x, ldx, M, out, ldo);
   if (rc != SKG_OK) return rc;
   rc = launch_tactic(h, h->plan[M], x, ldx, M, out, ldo, static_cast<cudaStream_t>(stream));
+  return rc == SKG_OK ? ok() : rc;
+}
+
+int skinny_gemm_run_residual(skinny_gemm_t h, const void* x, int64_t ldx, int64_t M,
+                             const void* residual, int64_t ldr, void* out, int64_t ldo,
+                             void* stream) {
+  int rc = validate_run(h, x, ldx, M, out, ldo);
+  if (rc != SKG_OK) return rc;
+  if (residual == nullptr) return fail(SKG_EINVAL, "null residual (use skinny_gemm_run)");
+  if (ldr < h->N) return fail(SKG_EINVAL, "residual row pitch %lld < N %lld",
+                               static_cast<long long>(ldr), static_cast<long long>(h->N));
+  if (reinterpret_cast<uintptr_t>(residual) % out_elem_bytes(h) != 0)
+    return fail(SKG_EALIGN, "residual must be aligned to its element size");
+  const char* r0 = static_cast<const char*>(residual);
+  const char* o0 = static_cast<const char*>(out);
+  const size_t esz = static_cast<size_t>(out_elem_bytes(h));
+  const char* r1 = r0 + (static_cast<size_t>(M - 1) * ldr + h->N) * esz;
+  const char* o1 = o0 + (static_cast<size_t>(M - 1) * ldo + h->N) * esz;
+  if (!(r0 == o0 && ldr == ldo) && r0 < o1 && o0 < r1)
+    return fail(SKG_EINVAL, "residual overlaps out without being exactly out (in place)");
+  rc = launch_tactic(h, h->plan[M], x, ldx, M, out, ldo, static_cast<cudaStream_t>(stream),
+                     residual, ldr);
   return rc == SKG_OK ? ok() : rc;
 }
 

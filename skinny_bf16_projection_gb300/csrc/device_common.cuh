@@ -217,6 +217,18 @@ template <>
 __device__ __forceinline__ __half to_out<__half>(float v) {
   return __float2half_rn(v);
 }
+__device__ __forceinline__ float from_out(float v) { return v; }
+__device__ __forceinline__ float from_out(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ float from_out(__half v) { return __half2float(v); }
+
+// out[t][n] = round(v + residual[t][n]) (residual optional, in the output type):
+// the residual joins the fp32 sum before the single rounding to the output type.
+template <typename OutT>
+__device__ __forceinline__ void store_out(const KParams& p, int t, int n, float v) {
+  if (p.residual != nullptr)
+    v += from_out(static_cast<const OutT*>(p.residual)[static_cast<int64_t>(t) * p.ldr + n]);
+  static_cast<OutT*>(p.out)[static_cast<int64_t>(t) * p.ldo + n] = to_out<OutT>(v);
+}
 
 // ---------------------------------------------------------------- mma.sync (legacy path)
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,

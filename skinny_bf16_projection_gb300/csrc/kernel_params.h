@@ -34,6 +34,9 @@ struct KParams {
   // stream-K kernel only: fp32 partial sums of split tiles and per-tile arrival counters
   float* workspace;       // [gridDim.x][2][TOK][128]
   uint32_t* counters;     // [ceil(N / 128)], zero between launches
+  // optional residual added before the output rounding: [M, ldr], output type
+  const void* residual;   // nullptr: none
+  int64_t ldr;
 };
 
 // Shared-memory footprint of one configuration (bytes, including 1 KB of

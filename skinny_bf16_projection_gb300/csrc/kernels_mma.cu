@@ -188,6 +188,7 @@ __global__ void __launch_bounds__(160) skinny_mma_kernel(const __grid_constant__
   }
 
   // ------------------------------------------------------------ epilogue
+  pdl_wait();  // every thread that reads residual / writes out is ordered after the previous grid
   if (csize > 1) cluster_wait_acquire();
   if (warp > 0) {
     // Accumulator fragment: c0,c1 -> row g, tokens 2q, 2q+1; c2,c3 -> row g+8.
@@ -226,7 +227,6 @@ __global__ void __launch_bounds__(160) skinny_mma_kernel(const __grid_constant__
   __syncthreads();
   if (csize > 1 && !mbar_wait_bounded<true>(recv_bar, 0, p.timeout_ns))
     report_status(p.status, kStatusTimeoutRecv);
-  OutT* const out = static_cast<OutT*>(p.out);
   const int nbase = n0 + static_cast<int>(rank) * RS;
   for (int idx = threadIdx.x; idx < RS * M; idx += blockDim.x) {
     const int rs2 = idx % RS;
@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(160) skinny_mma_kernel(const __grid_constant__
     float sum = 0.0f;
     for (uint32_t k = 0; k < csize; ++k) sum += red_g[(k * TOK + t) * RS + rs2];
     const int n = nbase + rs2;
-    if (n < p.N) out[static_cast<int64_t>(t) * p.ldo + n] = to_out<OutT>(sum);
+    if (n < p.N) store_out<OutT>(p, t, n, sum);
   }
   if (threadIdx.x == 0) {
     const int used = iters < S ? iters : S;

@@ -233,7 +233,6 @@ __global__ void __launch_bounds__(192) skinny_sk_kernel(const __grid_constant__ 
     const uint32_t quarter = warp & 3u;
     const int row = static_cast<int>(quarter * 32u + lane);
     const uint32_t ep_tid = threadIdx.x - 64u;  // 0..127
-    OutT* const out = static_cast<OutT*>(p.out);
     SegmentIter sg{u0, u1, kb};
     int t, ka, kend;
     for (int j = 0; sg.next(t, ka, kend); ++j) {
@@ -260,7 +259,7 @@ __global__ void __launch_bounds__(192) skinny_sk_kernel(const __grid_constant__ 
         if (n < p.N) {
 #pragma unroll
           for (int tk = 0; tk < TOK; ++tk)
-            if (tk < M) out[static_cast<int64_t>(tk) * p.ldo + n] = to_out<OutT>(v[tk]);
+            if (tk < M) store_out<OutT>(p, tk, n, v[tk]);
         }
         continue;
       }
@@ -328,11 +327,10 @@ __global__ void __launch_bounds__(192) skinny_sk_kernel(const __grid_constant__ 
             if (item >= items) continue;
             const int tk = item / (ROWS / 4);
             const int nb0 = t * ROWS + (item % (ROWS / 4)) * 4;
-            OutT* const o = out + static_cast<int64_t>(tk) * p.ldo + nb0;
-            if (nb0 + 0 < p.N) o[0] = to_out<OutT>(acc[ii].x);
-            if (nb0 + 1 < p.N) o[1] = to_out<OutT>(acc[ii].y);
-            if (nb0 + 2 < p.N) o[2] = to_out<OutT>(acc[ii].z);
-            if (nb0 + 3 < p.N) o[3] = to_out<OutT>(acc[ii].w);
+            if (nb0 + 0 < p.N) store_out<OutT>(p, tk, nb0 + 0, acc[ii].x);
+            if (nb0 + 1 < p.N) store_out<OutT>(p, tk, nb0 + 1, acc[ii].y);
+            if (nb0 + 2 < p.N) store_out<OutT>(p, tk, nb0 + 2, acc[ii].z);
+            if (nb0 + 3 < p.N) store_out<OutT>(p, tk, nb0 + 3, acc[ii].w);
           }
         }
         if (ep_tid == 0) p.counters[t] = 0u;  // ready for the next launch

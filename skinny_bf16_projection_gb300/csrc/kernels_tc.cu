@@ -185,14 +185,13 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
     for (int i = 0; i < 16; ++i) v[c * 16 + i] = iters > 0 ? t16[i] : 0.0f;
   }
   const int r = static_cast<int>(warp * 32u + lane);
-  OutT* const out = static_cast<OutT*>(p.out);
 
   if (csize == 1) {
     const int n = n0 + r;
     if (n < p.N) {
 #pragma unroll
       for (int t = 0; t < TOK; ++t)
-        if (t < M) out[static_cast<int64_t>(t) * p.ldo + n] = to_out<OutT>(v[t]);
+        if (t < M) store_out<OutT>(p, t, n, v[t]);
     }
   } else {
     cluster_wait_acquire();  // every peer's receive barrier is initialised
@@ -240,11 +239,10 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
       }
       const int n = nbase + rs2;
       if (n < p.N) {
-        OutT* const o = out + static_cast<int64_t>(4 * g) * p.ldo + n;
-        o[0] = to_out<OutT>(acc.x);
-        if (4 * g + 1 < M) o[p.ldo] = to_out<OutT>(acc.y);
-        if (4 * g + 2 < M) o[2 * p.ldo] = to_out<OutT>(acc.z);
-        if (4 * g + 3 < M) o[3 * p.ldo] = to_out<OutT>(acc.w);
+        store_out<OutT>(p, 4 * g, n, acc.x);
+        if (4 * g + 1 < M) store_out<OutT>(p, 4 * g + 1, n, acc.y);
+        if (4 * g + 2 < M) store_out<OutT>(p, 4 * g + 2, n, acc.z);
+        if (4 * g + 3 < M) store_out<OutT>(p, 4 * g + 3, n, acc.w);
       }
     }
   }

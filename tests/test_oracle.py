@@ -318,3 +318,27 @@ def test_bit_arrays_need_an_explicit_type():
     assert np.all(r0 == 0)
     with pytest.raises(TypeError):
         oracle.projection(torch.zeros(2, 8, dtype=torch.float16), torch.zeros(2, 8, dtype=torch.bfloat16))
+
+
+# ---------------------------------------------------------------- residual
+def test_residual_zero_x_returns_the_residual_exactly():
+    w = pin.weight(20, 64, seed=1)
+    r = (torch.randn(3, 20, generator=torch.Generator().manual_seed(2)) * 7).to(torch.bfloat16)
+    ref, s = oracle.projection_residual(torch.zeros(3, 64, dtype=torch.bfloat16), w, r)
+    assert np.array_equal(ref, r.double().numpy()) and np.all(s == 0)
+
+
+def test_residual_small_integers_exact():
+    x = pin.small_integers(4, 300, seed=5)
+    w = pin.small_integers(11, 300, seed=6)
+    r = pin.small_integers(4, 11, seed=7, lo=-1000, hi=1000).to(torch.float32)
+    ref, _ = oracle.projection_residual(x, w, r)
+    want = x.float().numpy().astype(np.int64) @ w.float().numpy().astype(np.int64).T + \
+        r.numpy().astype(np.int64)
+    assert np.array_equal(ref, want.astype(np.float64))
+
+
+def test_residual_shape_checked():
+    w = pin.weight(8, 16, seed=1)
+    with pytest.raises(ValueError):
+        oracle.projection_residual(torch.zeros(2, 16, dtype=torch.bfloat16), w, np.zeros((2, 9)))
