@@ -374,7 +374,58 @@ def other_workloads(torch, skg, pin, dev, l2, peak_gbs):
             p.close()
         del ws
         torch.cuda.empty_cache()
+    res["dependent chain: W[3584,7168] -> W[7168,3584] -> ... (each output feeds the next input)"] = \
+        dependent_chain(torch, skg, pin, dev, l2, peak_gbs)
     return res
+
+
+def dependent_chain(torch, skg, pin, dev, l2, peak_gbs):
+    """A layer-like chain of dependent projections (x -> W_b -> y -> W_a -> x' -> ...),
+    every weight read from HBM (rotated copies), as one CUDA graph: per projection
+    with programmatic dependent launch (the next projection's weight prologue overlaps
+    the previous one) and without it."""
+    stream = torch.cuda.current_stream(dev)
+    wbytes = 3584 * 7168 * 2
+    R = max(2, math.ceil(4.5 * l2 / wbytes))
+    wb0 = pin.weight(3584, 7168, seed=21).to(dev)
+    wa0 = pin.weight(7168, 3584, seed=22).to(dev)
+    wbs = [wb0] + [wb0.clone() for _ in range(R - 1)]
+    was = [wa0] + [wa0.clone() for _ in range(R - 1)]
+    x0 = pin.case(8, 7168, seed=23)[1].to(dev)
+    out = {}
+    tactics = {}
+    for pdl in (True, False):
+        pb = [skg.Projection(t, pdl=pdl) for t in wbs]
+        pa = [skg.Projection(t, pdl=pdl) for t in was]
+        for M in (1, 8):
+            if pdl:
+                pb[0].autotune([M])
+                pa[0].autotune([M])
+                tactics[M] = (pb[0].plan(M), pa[0].plan(M))
+            for q in pb:
+                q.set_tactic(M, tactics[M][0])
+            for q in pa:
+                q.set_tactic(M, tactics[M][1])
+            xs = x0[:M].contiguous()
+            y = torch.empty((M, 3584), dtype=torch.bfloat16, device=dev)
+            z = torch.empty((M, 7168), dtype=torch.bfloat16, device=dev)
+
+            def link(i):
+                if i % 2 == 0:
+                    pb[(i // 2) % R].run(xs if i == 0 else z, y)
+                else:
+                    pa[(i // 2) % R].run(y, z)
+            n = 2 * R * 2
+            us = graph_time_us(torch, stream, dev, link, n)
+            out[f"M{M}_{'pdl' if pdl else 'no_pdl'}"] = {
+                "us_per_projection": round(us, 3), "weight_GBps": round(wbytes / us / 1e3, 1),
+                "frac": round(wbytes / us / 1e3 / peak_gbs, 4),
+                "tactics": list(tactics[M])}
+        for q in pb + pa:
+            q.close()
+    del wbs, was
+    torch.cuda.empty_cache()
+    return out
 
 
 # ----------------------------------------------------------------------------- our arm

@@ -62,6 +62,11 @@ enum skinny_gemm_status {
 
 /* Flags for skinny_gemm_prepare_ex. */
 #define SKG_PREPARE_NO_TUNE_CACHE 0x1u /* ignore SKINNY_GEMM_TACTIC_FILE */
+/* Launch without programmatic dependent launch: each projection then starts
+ * only after the previous kernel on the stream has finished, so its weight
+ * prologue no longer overlaps that kernel (for measuring what the overlap
+ * hides, or for streams mixing kernels that must not overlap at all). */
+#define SKG_PREPARE_NO_PDL 0x2u
 
 /*
  * Prepare a projection for weight W[N, K] (packed, row pitch K).

@@ -49,7 +49,7 @@ class Projection:
     """
 
     def __init__(self, weight: torch.Tensor, out_dtype: torch.dtype | None = None, *,
-                 use_tactic_file: bool = True):
+                 use_tactic_file: bool = True, pdl: bool = True):
         if out_dtype is None:
             out_dtype = weight.dtype
         if not weight.is_cuda:
@@ -63,7 +63,7 @@ class Projection:
         with torch.cuda.device(weight.device):
             h = self._lib.skinny_gemm_prepare_ex(
                 ptr, weight.shape[0], weight.shape[1], ldw, _IN_CODES[weight.dtype],
-                _OUT_CODES[out_dtype], 0 if use_tactic_file else 1)
+                _OUT_CODES[out_dtype], (0 if use_tactic_file else 1) | (0 if pdl else 2))
         if not h:
             raise SkinnyGemmError(self._lib.skinny_gemm_last_status(), _native.last_error())
         self._h = ctypes.c_void_p(h)

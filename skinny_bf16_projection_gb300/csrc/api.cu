@@ -240,6 +240,7 @@ struct skinny_gemm_plan {
   void* out_stage = nullptr;
   uint64_t timeout_ns = 2000000000ull;
   int debug_count = 0;
+  bool pdl = true;  // programmatic dependent launch attribute on every launch
   uint64_t debug_timeout_ns = 0;
 };
 
@@ -375,9 +376,11 @@ int launch_tactic(skinny_gemm_plan* h, const Tactic& t, const void* x, int64_t l
   // real clusters.
   cudaLaunchAttribute attrs[2];
   int na = 0;
-  attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attrs[na].val.programmaticStreamSerializationAllowed = 1;
-  ++na;
+  if (h->pdl) {
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
   if (tactic_cluster(t) > 1) {
     attrs[na].id = cudaLaunchAttributeClusterDimension;
     attrs[na].val.clusterDim.x = static_cast<unsigned>(tactic_cluster(t));
@@ -662,6 +665,7 @@ skinny_gemm_t skinny_gemm_prepare_ex(const void* W, int64_t N, int64_t K, int64_
     return nullptr;
   }
   for (int m = 1; m <= SKINNY_GEMM_MAX_M; ++m) h->plan[m] = default_tactic(h, m);
+  h->pdl = !(flags & SKG_PREPARE_NO_PDL);
   if (!(flags & SKG_PREPARE_NO_TUNE_CACHE)) load_tactic_file(h);
   if (const char* f = getenv("SKINNY_GEMM_FORCE_TACTIC")) {
     Tactic t;

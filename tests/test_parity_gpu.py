@@ -330,3 +330,21 @@ def test_stream_k_every_tactic_full_size(N):
                     y = run_proj(proj, xd[:M], odt)
                     assert_parity(y, ref[:M], s[:M], f"N={N} M={M} {odt} {t}")
         proj.check_status()
+
+
+def test_dependent_chain_without_pdl_matches_with_pdl():
+    """The same 8-link dependent chain launched without programmatic dependent
+    launch gives the same bits as with it."""
+    D = 2048
+    w = pin.weight(D, D, seed=9, std=1.0 / np.sqrt(D))
+    x0 = pin.case(8, D, seed=10)[1][:4].to(DEV)
+    results = []
+    for pdl in (True, False):
+        proj = skg().Projection(w.to(DEV), use_tactic_file=False, pdl=pdl)
+        bufs = [x0] + [torch.empty((4, D), dtype=torch.bfloat16, device=DEV) for _ in range(8)]
+        for i in range(8):
+            proj.run(bufs[i], bufs[i + 1])
+        torch.cuda.synchronize()
+        results.append(bufs[-1].clone())
+        proj.close()
+    assert torch.equal(results[0], results[1])
