@@ -248,6 +248,8 @@ def reference_arm(args, rank, world):
 def graph_time_us(torch, stream, dev, fn, n_launch: int, reps: int = 5) -> float:
     """Per-call time of fn(i) for i in range(n_launch), captured as one CUDA graph and
     replayed (best of reps), in microseconds per call."""
+    fn(0)  # eager warm-up: library handles (e.g. cuBLAS for the context rows) are created here
+    torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     side = torch.cuda.Stream(dev)
     side.wait_stream(stream)
@@ -280,10 +282,10 @@ def other_workloads(torch, skg, pin, dev, l2, peak_gbs):
         K = 7168
         wbytes = N * K * 2
         R = max(2, math.ceil(4.5 * l2 / wbytes))
-        w, x = pin.case(N, K, seed=0)
+        w, x = pin.case(N, K, seed=0, max_tokens=256)
         ws = [w.to(dev)]
         ws += [ws[0].clone() for _ in range(R - 1)]
-        Ms = (1, 2, 4, 8, 16, 32, 48, 64)
+        Ms = (1, 2, 4, 8, 16, 32, 48, 64, 128, 256)
         p16 = [skg.Projection(t) for t in ws]
         p32 = [skg.Projection(t, torch.float32) for t in ws]
         p16[0].autotune(list(Ms))
@@ -304,6 +306,15 @@ def other_workloads(torch, skg, pin, dev, l2, peak_gbs):
                 entry[f"M{M}_{'bf16' if odt == torch.bfloat16 else 'fp32'}"] = {
                     "us": round(us, 3), "weight_GBps": round(gbs, 1),
                     "frac": round(gbs / peak_gbs, 4), "tactic": projs[0].plan(M)}
+        # context only (not part of this library): cuBLAS through torch.mm, same rotation
+        for M in (1, 8, 32, 64, 128, 256):
+            out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            xm = xd[:M].contiguous()
+            us = graph_time_us(torch, stream, dev,
+                               lambda i: torch.mm(xm, ws[i % R].t(), out=out),
+                               R * max(1, math.ceil(48 / R)))
+            entry[f"M{M}_bf16_context_torch_mm"] = {"us": round(us, 3),
+                                                    "weight_GBps": round(wbytes / us / 1e3, 1)}
         res[f"W[{N},{K}] rotated x{R}"] = entry
         if N == 3584:
             # fused residual epilogue, in place: out = x @ W^T + out

@@ -1,7 +1,7 @@
 /*
  * skinny_gemm.h — C ABI of the GB300 (sm_103a) skinny BF16 decode projection.
  *
- *   out[M, N] = x[M, K] @ W[N, K]^T,   1 <= M <= 64 tokens,
+ *   out[M, N] = x[M, K] @ W[N, K]^T,   1 <= M <= 256 tokens (decode: 1..64),
  *   x and W bf16, accumulation fp32, out bf16 (round to nearest even) or fp32.
  *
  * Operation: page "vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.
@@ -36,7 +36,7 @@ extern "C" {
 #endif
 
 #define SKINNY_GEMM_ABI_VERSION 1
-#define SKINNY_GEMM_MAX_M 64
+#define SKINNY_GEMM_MAX_M 256
 
 typedef struct skinny_gemm_plan* skinny_gemm_t; /* opaque prepared projection */
 
@@ -53,7 +53,7 @@ enum skinny_gemm_status {
   SKG_OK = 0,
   SKG_EINVAL = 1,          /* bad handle, shape, pitch or dtype */
   SKG_EALIGN = 2,          /* pointer or row pitch not 16-byte aligned */
-  SKG_EUNSUPPORTED_M = 3,  /* M outside 1..64: caller falls back */
+  SKG_EUNSUPPORTED_M = 3,  /* M outside 1..256: caller falls back */
   SKG_EDEVICE = 4,         /* current device is not sm_103 */
   SKG_ECUDA = 5,           /* a CUDA runtime/driver call failed */
   SKG_ECAPTURING = 6,      /* prepare/autotune called while the stream captures */
@@ -72,7 +72,7 @@ enum skinny_gemm_status {
  * Prepare a projection for weight W[N, K] (packed, row pitch K).
  * Validates W, encodes its TMA maps (box {64, rows}, 128-byte swizzle,
  * 256-byte L2 promotion, out-of-bounds zero fill; projection page,
- * weight_map) and builds the {M: tactic} plan for M = 1..64 (low_latency_gemm
+ * weight_map) and builds the {M: tactic} plan for M = 1..256 (low_latency_gemm
  * page, module docstring: the static part of the choice is resolved once, the
  * per-call path is one lookup).  A tactic for M is the one of the smallest
  * token tile >= M (glm5next gemm page, Projection.__init__).
@@ -172,7 +172,7 @@ int skinny_gemm_run_overlap(skinny_gemm_t h_main, skinny_gemm_t h_fa, skinny_gem
  */
 int skinny_gemm_autotune(skinny_gemm_t h, const int64_t* Ms, int nM, void* stream);
 
-/* Force the tactic used for token count M (1..64), given as the string
+/* Force the tactic used for token count M (1..256), given as the string
  * skinny_gemm_plan_query prints.  EINVAL if it does not parse or does not fit
  * this weight and M. */
 int skinny_gemm_set_tactic(skinny_gemm_t h, int64_t M, const char* tactic);

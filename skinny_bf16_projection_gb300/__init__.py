@@ -41,7 +41,7 @@ def _matrix(t: torch.Tensor, name: str) -> tuple[int, int]:
 
 
 class Projection:
-    """A prepared projection ``out = x @ weight.T`` for 1..64 tokens.
+    """A prepared projection ``out = x @ weight.T`` for 1..256 tokens (decode: 1..64).
 
     ``weight`` [N, K] (bf16 or fp16, CUDA, unit inner stride) is borrowed: this
     object keeps a reference so it stays alive, and it must not be moved or

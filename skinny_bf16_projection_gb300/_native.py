@@ -17,7 +17,7 @@ SKG_OK, SKG_EINVAL, SKG_EALIGN, SKG_EUNSUPPORTED_M = 0, 1, 2, 3
 SKG_EDEVICE, SKG_ECUDA, SKG_ECAPTURING, SKG_ETIMEOUT = 4, 5, 6, 7
 STATUS_NAMES = {0: "OK", 1: "EINVAL", 2: "EALIGN", 3: "EUNSUPPORTED_M", 4: "EDEVICE",
                 5: "ECUDA", 6: "ECAPTURING", 7: "ETIMEOUT"}
-MAX_M = 64
+MAX_M = 256
 
 # (name, restype, argtypes) for every function the header declares.
 _i64, _int, _vp, _cp, _u64, _sz = (ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,

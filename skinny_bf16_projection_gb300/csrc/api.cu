@@ -215,7 +215,7 @@ uint64_t env_u64(const char* name, uint64_t dflt) {
   return strtoull(v, nullptr, 10);
 }
 
-const int kTcToks[] = {16, 32, 64};
+const int kTcToks[] = {16, 32, 64, 128, 256};
 const int kMmaToks[] = {8, 16, 32};
 const int kClusters[] = {1, 2, 4, 8, 16};
 
@@ -253,7 +253,7 @@ int ntiles_of(const skinny_gemm_plan* h, const Tactic& t) {
 }
 uint32_t tactic_smem(const Tactic& t) {
   if (t.variant == kVariantSk) return sk_smem_bytes(t.tok, t.nbox, t.stages);
-  if (t.variant == kVariantTc) return tc_smem_bytes(t.tok, t.nbox, t.stages);
+  if (t.variant == kVariantTc) return tc_smem_bytes(t.tok, t.nbox, t.stages, t.cl);
   return smem_bytes(t.rows, t.tok, t.nbox, t.stages);
 }
 // CTAs launched: row tiles x cluster size, or (stream-K) CTAs-per-SM x SMs,
@@ -447,8 +447,9 @@ std::vector<Tactic> candidates(const skinny_gemm_plan* h, int64_t M) {
   std::vector<Tactic> out;
   for (int variant : {kVariantTc, kVariantMma, kVariantSk}) {
     const int* toks = variant == kVariantMma ? kMmaToks : kTcToks;
+    const int ntok = variant == kVariantMma ? 3 : (variant == kVariantSk ? 3 : 5);
     int tok = 0;
-    for (int i = 0; i < 3; ++i)
+    for (int i = 0; i < ntok; ++i)
       if (toks[i] >= M) {
         tok = toks[i];
         break;
@@ -517,8 +518,12 @@ Tactic default_tactic(const skinny_gemm_plan* h, int64_t M) {
     t = with_cluster(Tactic{kVariantMma, 64, 16, 2, 2, 1, 0});
   else if (M <= 32)
     t = with_cluster(Tactic{kVariantTc, 128, 32, 2, 2, 1, 0});
-  else
+  else if (M <= 64)
     t = with_cluster(Tactic{kVariantTc, 128, 64, 1, 3, 1, 0});
+  else if (M <= 128)
+    t = with_cluster(Tactic{kVariantTc, 128, 128, 1, 2, 1, 0});
+  else
+    t = with_cluster(Tactic{kVariantTc, 128, 256, 1, 2, 1, 0});
   if (t.valid()) return t;
   for (int tok : kTcToks)
     if (tok >= M) {

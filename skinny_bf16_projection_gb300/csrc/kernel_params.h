@@ -76,8 +76,9 @@ const KernelEntry* sk_kernel_table(int* count);
 __host__ __device__ constexpr uint32_t tc_red_bytes(int tok) {
   return static_cast<uint32_t>(128 * (tok + 4) * 4);
 }
-__host__ __device__ constexpr uint32_t tc_smem_bytes(int tok, int nbox, int stages) {
-  return kSmemAlign + stages * stage_bytes(128, tok, nbox) + tc_red_bytes(tok) +
+// (The receive buffer exists only for clusters of more than one CTA.)
+__host__ __device__ constexpr uint32_t tc_smem_bytes(int tok, int nbox, int stages, int cluster) {
+  return kSmemAlign + stages * stage_bytes(128, tok, nbox) + (cluster > 1 ? tc_red_bytes(tok) : 0u) +
          static_cast<uint32_t>((2 * stages + 4) * 8) + 16;
 }
 

@@ -38,17 +38,18 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
   constexpr uint32_t kWBox = ROWS * kBoxRowBytes;
   constexpr uint32_t kXBox = TOK * kBoxRowBytes;
   constexpr uint32_t kStage = stage_bytes(ROWS, TOK, NBOX);
-  constexpr uint32_t kTmemCols = TOK <= 32 ? 32u : 64u;
+  constexpr uint32_t kTmemCols = TOK <= 32 ? 32u : static_cast<uint32_t>(TOK);
   constexpr uint32_t kIdesc = mma_idesc<kFp16>(ROWS, TOK);
-  static_assert(TOK % 16 == 0 && TOK >= 16 && TOK <= 64, "M=128 MMA needs N % 16 == 0");
+  static_assert(TOK % 16 == 0 && TOK >= 16 && TOK <= 256, "M=128 MMA needs N % 16 == 0, N <= 256");
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + kSmemAlign - 1) & ~static_cast<uint32_t>(kSmemAlign - 1);
   uint8_t* const gbase = smem_raw + (base - raw);
   const int S = p.stages;
+  const uint32_t csize = cluster_nctarank();
   const uint32_t red = base + static_cast<uint32_t>(S) * kStage;
-  const uint32_t bars = red + tc_red_bytes(TOK);
+  const uint32_t bars = red + (csize > 1 ? tc_red_bytes(TOK) : 0u);
   const uint32_t done_bar = bars + 8u * (2 * S);
   const uint32_t recv_bar = done_bar + 8u;
   const uint32_t dbg_bar = done_bar + 16u;
@@ -72,7 +73,6 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
     return;
   }
 
-  const uint32_t csize = cluster_nctarank();
   const uint32_t rank = cluster_ctarank();
   const int n0 = static_cast<int>(blockIdx.x / csize) * ROWS;
   const int kb0 = static_cast<int>(static_cast<int64_t>(rank) * p.kboxes / csize);
@@ -175,23 +175,31 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
   pdl_wait();
   if (!mbar_wait_bounded(done_bar, 0, p.timeout_ns)) report_status(p.status, kStatusTimeoutDone);
   tc_fence_after_sync();
-  float v[TOK];
+  // The accumulator is read 32 TMEM columns (tokens) at a time, so registers
+  // stay bounded for token tiles up to 256.
+  constexpr int CH = TOK < 32 ? TOK : 32;
   const uint32_t row_taddr = tmem + ((warp * 32u) << 16);
-#pragma unroll
-  for (int c = 0; c < TOK / 16; ++c) {
-    float t16[16];
-    tmem_ld_32x32b_x16(row_taddr + static_cast<uint32_t>(c * 16), t16);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[c * 16 + i] = iters > 0 ? t16[i] : 0.0f;
-  }
   const int r = static_cast<int>(warp * 32u + lane);
+  auto load_chunk = [&](int c0, float (&v)[CH]) {
+#pragma unroll
+    for (int c = 0; c < CH / 16; ++c) {
+      float t16[16];
+      tmem_ld_32x32b_x16(row_taddr + static_cast<uint32_t>(c0 + c * 16), t16);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[c * 16 + i] = iters > 0 ? t16[i] : 0.0f;
+    }
+  };
 
   if (csize == 1) {
     const int n = n0 + r;
-    if (n < p.N) {
+    for (int c0 = 0; c0 < TOK && c0 < M; c0 += CH) {
+      float v[CH];
+      load_chunk(c0, v);
+      if (n < p.N) {
 #pragma unroll
-      for (int t = 0; t < TOK; ++t)
-        if (t < M) store_out<OutT>(p, t, n, v[t]);
+        for (int i = 0; i < CH; ++i)
+          if (c0 + i < M) store_out<OutT>(p, c0 + i, n, v[i]);
+      }
     }
   } else {
     cluster_wait_acquire();  // every peer's receive barrier is initialised
@@ -202,21 +210,23 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
     const uint32_t owner = static_cast<uint32_t>(r / RS);
     const int rs = r % RS;
     const uint32_t row_off = ((rank * RS + rs) * TP) * 4u;
-    if (owner == rank) {
+    const uint32_t raddr = owner == rank ? 0u : mapa_shared(red + row_off, owner);
+    const uint32_t rbar = owner == rank ? 0u : mapa_shared(recv_bar, owner);
+    for (int c0 = 0; c0 < TOK && c0 < M; c0 += CH) {
+      float v[CH];
+      load_chunk(c0, v);
 #pragma unroll
-      for (int g = 0; g < TOK / 4; ++g)
-        if (g < MG)
-          asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(red + row_off + g * 16u),
+      for (int g = 0; g < CH / 4; ++g) {
+        const int gg = c0 / 4 + g;
+        if (gg >= MG) continue;
+        if (owner == rank)
+          asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(red + row_off + gg * 16u),
                        "f"(v[4 * g]), "f"(v[4 * g + 1]), "f"(v[4 * g + 2]), "f"(v[4 * g + 3])
                        : "memory");
-    } else {
-      const uint32_t raddr = mapa_shared(red + row_off, owner);
-      const uint32_t rbar = mapa_shared(recv_bar, owner);
-#pragma unroll
-      for (int g = 0; g < TOK / 4; ++g)
-        if (g < MG)
-          st_async_v4(raddr + static_cast<uint32_t>(g * 16), v[4 * g], v[4 * g + 1], v[4 * g + 2],
+        else
+          st_async_v4(raddr + static_cast<uint32_t>(gg * 16), v[4 * g], v[4 * g + 1], v[4 * g + 2],
                       v[4 * g + 3], rbar);
+      }
     }
     __syncthreads();
     if (!mbar_wait_bounded<true>(recv_bar, 0, p.timeout_ns))
@@ -273,13 +283,15 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
       SKG_TC_ENTRY(16, 4, OUTT, OUTCODE, false), SKG_TC_ENTRY(32, 1, OUTT, OUTCODE, false), \
       SKG_TC_ENTRY(32, 2, OUTT, OUTCODE, false), SKG_TC_ENTRY(32, 4, OUTT, OUTCODE, false), \
       SKG_TC_ENTRY(64, 1, OUTT, OUTCODE, false), SKG_TC_ENTRY(64, 2, OUTT, OUTCODE, false), \
-      SKG_TC_ENTRY(64, 4, OUTT, OUTCODE, false)
+      SKG_TC_ENTRY(64, 4, OUTT, OUTCODE, false), SKG_TC_ENTRY(128, 1, OUTT, OUTCODE, false), \
+      SKG_TC_ENTRY(128, 2, OUTT, OUTCODE, false), SKG_TC_ENTRY(256, 1, OUTT, OUTCODE, false)
 
 // fp16 operands: one or two boxes per stage.
 #define SKG_TC_ROW16(OUTT, OUTCODE)                                                         \
   SKG_TC_ENTRY(16, 1, OUTT, OUTCODE, true), SKG_TC_ENTRY(16, 2, OUTT, OUTCODE, true),       \
       SKG_TC_ENTRY(32, 1, OUTT, OUTCODE, true), SKG_TC_ENTRY(32, 2, OUTT, OUTCODE, true),   \
-      SKG_TC_ENTRY(64, 1, OUTT, OUTCODE, true), SKG_TC_ENTRY(64, 2, OUTT, OUTCODE, true)
+      SKG_TC_ENTRY(64, 1, OUTT, OUTCODE, true), SKG_TC_ENTRY(64, 2, OUTT, OUTCODE, true),   \
+      SKG_TC_ENTRY(128, 1, OUTT, OUTCODE, true), SKG_TC_ENTRY(256, 1, OUTT, OUTCODE, true)
 
 static const KernelEntry kTcTable[] = {SKG_TC_ROW(__nv_bfloat16, 0), SKG_TC_ROW(float, 2),
                                        SKG_TC_ROW16(__half, 1), SKG_TC_ROW16(float, 2)};

@@ -268,7 +268,7 @@ def test_error_codes():
     out = torch.empty(64, 256 + 8, device=DEV, dtype=torch.bfloat16)
     st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     assert lib.skinny_gemm_run(proj._h, x.data_ptr(), 0, out.data_ptr(), st) == nat.SKG_EUNSUPPORTED_M
-    assert lib.skinny_gemm_run(proj._h, x.data_ptr(), 65, out.data_ptr(), st) == nat.SKG_EUNSUPPORTED_M
+    assert lib.skinny_gemm_run(proj._h, x.data_ptr(), 257, out.data_ptr(), st) == nat.SKG_EUNSUPPORTED_M
     assert lib.skinny_gemm_run(proj._h, x.data_ptr() + 2, 4, out.data_ptr(), st) == nat.SKG_EALIGN
     assert lib.skinny_gemm_run(proj._h, x.data_ptr(), 4, out.data_ptr() + 8, st) == nat.SKG_EALIGN
     assert lib.skinny_gemm_run_strided(proj._h, x.data_ptr(), 1000, 4, out.data_ptr(), 256, st) \

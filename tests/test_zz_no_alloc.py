@@ -71,7 +71,7 @@ def test_noalloc_rejects_bad_requests(skg):
     st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     args = lambda M, xp=x.data_ptr(), wp=w.data_ptr(): (wp, 256, 1024, 1024, nat.SKG_BF16, xp,
                                                        1024, M, out.data_ptr(), 256, st)
-    assert lib.skinny_gemm_run_noalloc(*args(65)) == nat.SKG_EUNSUPPORTED_M
+    assert lib.skinny_gemm_run_noalloc(*args(nat.MAX_M + 1)) == nat.SKG_EUNSUPPORTED_M
     assert lib.skinny_gemm_run_noalloc(*args(0)) == nat.SKG_EUNSUPPORTED_M
     assert lib.skinny_gemm_run_noalloc(*args(4, xp=x.data_ptr() + 2)) == nat.SKG_EALIGN
     assert lib.skinny_gemm_run_noalloc(*args(4, wp=w.data_ptr() + 2)) == nat.SKG_EALIGN
