@@ -14,7 +14,7 @@ import torch
 from . import _native
 from ._native import MAX_M, SkinnyGemmError
 
-__all__ = ["Projection", "run_overlap", "SkinnyGemmError", "MAX_M", "library_path"]
+__all__ = ["Projection", "run_overlap", "tune_overlap", "SkinnyGemmError", "MAX_M", "library_path"]
 
 _OUT_CODES = {torch.bfloat16: _native.SKG_BF16, torch.float16: _native.SKG_FP16,
               torch.float32: _native.SKG_FP32}
@@ -174,3 +174,14 @@ def run_overlap(main: Projection, fa: Projection, fb: Projection, x: torch.Tenso
         main._h, fa._h, fb._h, chain, x.data_ptr(), M, out_main.data_ptr(), fa_out.data_ptr(),
         out_fb.data_ptr(), _stream_ptr(stream), _stream_ptr(aux_stream),
         ctypes.c_void_p(int(events[0].cuda_event)), ctypes.c_void_p(int(events[1].cuda_event))))
+
+
+def tune_overlap(main: Projection, fa: Projection, fb: Projection, Ms: Iterable[int], *,
+                 chain: int = 1, stream=None) -> None:
+    """Pick fa's tactic for each M by timing the whole two-stream step (see
+    skinny_gemm_autotune_overlap); main and fb keep their plans."""
+    ms = list(Ms)
+    arr = (ctypes.c_int64 * len(ms))(*ms)
+    with torch.cuda.device(main.device):
+        _native.check(_native.lib().skinny_gemm_autotune_overlap(
+            main._h, fa._h, fb._h, chain, arr, len(ms), _stream_ptr(stream)))

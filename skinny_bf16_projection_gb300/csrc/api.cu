@@ -816,6 +816,158 @@ int skinny_gemm_run_overlap(skinny_gemm_t h_main, skinny_gemm_t h_fa, skinny_gem
   return ok();
 }
 
+int skinny_gemm_autotune_overlap(skinny_gemm_t h_main, skinny_gemm_t h_fa, skinny_gemm_t h_fb,
+                                 int chain, const int64_t* Ms, int nM, void* stream) {
+  if (h_main == nullptr || h_fa == nullptr || h_fb == nullptr) return fail(SKG_EINVAL, "null handle");
+  if (chain < 1) return fail(SKG_EINVAL, "chain must be >= 1");
+  if (h_fa->K != h_main->K || h_fb->K != h_fa->N || h_fa->out_dtype != SKG_BF16 ||
+      h_main->dtype != h_fa->dtype)
+    return fail(SKG_EINVAL, "handles do not form an overlap step (see skinny_gemm_run_overlap)");
+  if (chain > 1 && (h_fb->out_dtype != SKG_BF16 || h_fb->N < h_fb->K))
+    return fail(SKG_EINVAL, "a chain needs bf16 F_B output with N_fb >= K_fb");
+  if (Ms == nullptr || nM < 1) return fail(SKG_EINVAL, "no token counts to tune");
+  for (int i = 0; i < nM; ++i)
+    if (Ms[i] < 1 || Ms[i] > SKINNY_GEMM_MAX_M)
+      return fail(SKG_EUNSUPPORTED_M, "M = %lld outside 1..%d", static_cast<long long>(Ms[i]),
+                  SKINNY_GEMM_MAX_M);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(st, &cs);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+  if (cs != cudaStreamCaptureStatusNone)
+    return fail(SKG_ECAPTURING, "autotune must run before CUDA graph capture");
+  e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+
+  // The whole step is timed as a CUDA graph of back-to-back steps; the main
+  // projection rotates over scratch copies of its weight layout (>= 4.5x L2).
+  const size_t wbytes = static_cast<size_t>(h_main->N) * h_main->ldw * 2;
+  const size_t l2 = static_cast<size_t>(std::max(h_main->dev->l2_bytes, 1 << 20));
+  const int R = static_cast<int>(std::min<size_t>(64, std::max<size_t>(2, (9 * l2 / 2 + wbytes - 1) / wbytes)));
+  const int L = R * std::max(1, (12 + R - 1) / R);
+  void *rot = nullptr, *xb = nullptr, *om = nullptr, *fo = nullptr, *fbo = nullptr;
+  cudaStream_t ts = nullptr, as = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr, e0 = nullptr, e1 = nullptr;
+  auto cleanup = [&]() {
+    if (ts) cudaStreamSynchronize(ts);
+    if (as) cudaStreamSynchronize(as);
+    for (void* p : {rot, xb, om, fo, fbo})
+      if (p) cudaFree(p);
+    for (cudaEvent_t ev : {fork, join, e0, e1})
+      if (ev) cudaEventDestroy(ev);
+    if (ts) cudaStreamDestroy(ts);
+    if (as) cudaStreamDestroy(as);
+  };
+  int lo_pri = 0, hi_pri = 0;
+  cudaDeviceGetStreamPriorityRange(&lo_pri, &hi_pri);
+  const size_t mx = SKINNY_GEMM_MAX_M;
+  if ((e = cudaMalloc(&rot, wbytes * R)) != cudaSuccess ||
+      (e = cudaMalloc(&xb, mx * h_main->K * 2)) != cudaSuccess ||
+      (e = cudaMalloc(&om, mx * h_main->N * out_elem_bytes(h_main))) != cudaSuccess ||
+      (e = cudaMalloc(&fo, mx * h_fa->N * 2)) != cudaSuccess ||
+      (e = cudaMalloc(&fbo, static_cast<size_t>(chain) * mx * h_fb->N * out_elem_bytes(h_fb))) != cudaSuccess ||
+      (e = cudaMemset(rot, 0, wbytes * R)) != cudaSuccess ||
+      (e = cudaMemset(xb, 0, mx * h_main->K * 2)) != cudaSuccess ||
+      (e = cudaMemset(fo, 0, mx * h_fa->N * 2)) != cudaSuccess ||
+      (e = cudaStreamCreateWithFlags(&ts, cudaStreamNonBlocking)) != cudaSuccess ||
+      (e = cudaStreamCreateWithPriority(&as, cudaStreamNonBlocking, hi_pri)) != cudaSuccess ||
+      (e = cudaEventCreateWithFlags(&fork, cudaEventDisableTiming)) != cudaSuccess ||
+      (e = cudaEventCreateWithFlags(&join, cudaEventDisableTiming)) != cudaSuccess ||
+      (e = cudaEventCreate(&e0)) != cudaSuccess || (e = cudaEventCreate(&e1)) != cudaSuccess) {
+    cleanup();
+    return cuda_fail(e, "autotune_overlap setup");
+  }
+  std::vector<skinny_gemm_plan> shadow(R, *h_main);
+  for (int r = 0; r < R; ++r) {
+    skinny_gemm_plan& sh = shadow[r];
+    sh.W = static_cast<char*>(rot) + r * wbytes;
+    sh.debug_count = 0;
+    sh.x_stage = sh.out_stage = nullptr;
+    if (encode_map(&sh.wmap64, sh.W, h_main->N, h_main->K, h_main->ldw, 64, h_main->dtype,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B) != SKG_OK ||
+        encode_map(&sh.wmap128, sh.W, h_main->N, h_main->K, h_main->ldw, 128, h_main->dtype,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B) != SKG_OK) {
+      const int code = g_last_status;
+      cleanup();
+      return code;
+    }
+  }
+  int rc = SKG_OK;
+  std::vector<int64_t> tuned;
+  for (int i = 0; i < nM && rc == SKG_OK; ++i) {
+    const int64_t M = Ms[i];
+    const Tactic keep = h_fa->plan[M];
+    double best_us = 1e30;
+    Tactic best;
+    for (const Tactic& t : candidates(h_fa, M)) {
+      rc = ensure_workspace(h_fa, t);
+      if (rc != SKG_OK) break;
+      h_fa->plan[M] = t;
+      cudaGraph_t graph = nullptr;
+      cudaGraphExec_t exec = nullptr;
+      e = cudaStreamBeginCapture(ts, cudaStreamCaptureModeThreadLocal);
+      if (e != cudaSuccess) {
+        rc = cuda_fail(e, "cudaStreamBeginCapture(autotune_overlap)");
+        break;
+      }
+      for (int l = 0; l < L && rc == SKG_OK; ++l)
+        rc = skinny_gemm_run_overlap(&shadow[l % R], h_fa, h_fb, chain, xb, M, om, fo, fbo, ts, as,
+                                     fork, join);
+      e = cudaStreamEndCapture(ts, &graph);
+      if (rc != SKG_OK || e != cudaSuccess) {
+        if (graph) cudaGraphDestroy(graph);
+        if (rc == SKG_OK) rc = cuda_fail(e, "cudaStreamEndCapture(autotune_overlap)");
+        break;
+      }
+      e = cudaGraphInstantiate(&exec, graph, 0);
+      if (e != cudaSuccess) {
+        cudaGraphDestroy(graph);
+        rc = cuda_fail(e, "cudaGraphInstantiate(autotune_overlap)");
+        break;
+      }
+      float best_ms = 1e30f;
+      e = cudaGraphLaunch(exec, ts);
+      for (int r = 0; r < 3 && e == cudaSuccess; ++r) {
+        cudaEventRecord(e0, ts);
+        e = cudaGraphLaunch(exec, ts);
+        cudaEventRecord(e1, ts);
+        if (e == cudaSuccess) e = cudaEventSynchronize(e1);
+        float ms = 0;
+        if (e == cudaSuccess && cudaEventElapsedTime(&ms, e0, e1) == cudaSuccess)
+          best_ms = std::min(best_ms, ms);
+      }
+      cudaGraphExecDestroy(exec);
+      cudaGraphDestroy(graph);
+      if (e != cudaSuccess) {
+        rc = cuda_fail(e, "autotune_overlap timing");
+        break;
+      }
+      const double us = 1000.0 * best_ms / L;
+      if (log_enabled())
+        fprintf(stderr, "[skinny_gemm] tune overlap M=%lld F_A %s: step %.3f us\n",
+                static_cast<long long>(M), tactic_str(t).c_str(), us);
+      if (us < best_us) {
+        best_us = us;
+        best = t;
+      }
+    }
+    h_fa->plan[M] = (rc == SKG_OK && best.valid()) ? best : keep;
+    if (rc == SKG_OK && best.valid()) tuned.push_back(M);
+  }
+  cleanup();
+  if (rc != SKG_OK) return rc;
+  std::sort(tuned.begin(), tuned.end());
+  for (int m = 1; m <= SKINNY_GEMM_MAX_M; ++m) {
+    if (std::binary_search(tuned.begin(), tuned.end(), static_cast<int64_t>(m))) continue;
+    for (int64_t mp : tuned)
+      if (mp >= m) {
+        if (tactic_fits(h_fa, h_fa->plan[mp], m, nullptr)) h_fa->plan[m] = h_fa->plan[mp];
+        break;
+      }
+  }
+  return ok();
+}
+
 int skinny_gemm_set_tactic(skinny_gemm_t h, int64_t M, const char* tactic) {
   if (check_handle(h) != SKG_OK) return SKG_EINVAL;
   if (M < 1 || M > SKINNY_GEMM_MAX_M)

@@ -100,3 +100,30 @@ def test_overlap_rejects_mismatched_handles(setup):
     with pytest.raises(skg.SkinnyGemmError):  # F_B's K (128) must equal F_A's N
         skg.run_overlap(st["main"], st["fb"], st["fb"], st["x"][:M], out_main, fa_out, out_fb,
                         aux_stream=aux, events=events)
+
+
+def test_overlap_tuned_fa_plan_keeps_parity(setup):
+    """skinny_gemm_autotune_overlap times each F_A candidate inside the whole
+    step and installs the fastest; the step must stay correct with it, and
+    the main and F_B plans must not change."""
+    st = setup
+    skg = st["skg"]
+    fa = skg.Projection(st["main"].weight[:128], use_tactic_file=False)
+    chain = 4
+    main_before = [st["main"].plan(M) for M in (1, 8, 32)]
+    fb_before = [st["fb"].plan(M) for M in (1, 8, 32)]
+    skg.tune_overlap(st["main"], fa, st["fb"], [1, 8, 32], chain=chain)
+    assert [st["main"].plan(M) for M in (1, 8, 32)] == main_before
+    assert [st["fb"].plan(M) for M in (1, 8, 32)] == fb_before
+    aux = torch.cuda.Stream(priority=-1)
+    events = (torch.cuda.Event(), torch.cuda.Event())
+    for M in (1, 5, 8, 32):
+        out_main = torch.empty((M, 6288), dtype=torch.bfloat16, device=DEV)
+        fa_out = torch.empty((M, 128), dtype=torch.bfloat16, device=DEV)
+        out_fb = torch.empty((chain, M, 1536), dtype=torch.bfloat16, device=DEV)
+        skg.run_overlap(st["main"], fa, st["fb"], st["x"][:M], out_main, fa_out, out_fb,
+                        chain=chain, aux_stream=aux, events=events)
+        torch.cuda.synchronize()
+        assert_parity(out_main, st["ref"][:M], st["s"][:M], f"tuned main M={M}")
+        check_links(st, M, fa_out, out_fb, chain)
+    fa.close()
