@@ -105,16 +105,20 @@ int encode_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, in
 // parts per row tile (mode 1, "p").
 struct Tactic {
   int variant = 0, rows = 0, tok = 0, nbox = 0, stages = 0, cl = 0, mode = 0;
+  int lt = 0;  // k >= 1: launch dependents only with k-1 stages' loads left to issue (mma / tc)
   bool valid() const { return variant != 0; }
 };
 
-// "tc:r128:t16:b2:s4:c8" (c = cluster size) or "sk:r128:t16:b2:s5:g1" (g = CTAs per SM).
+// "tc:r128:t16:b2:s4:c8" (c = cluster size) or "sk:r128:t16:b2:s5:g1" (g = CTAs per SM),
+// with ":d<k>" appended for a late PDL trigger (mma / tc).
 std::string tactic_str(const Tactic& t) {
   char b[96];
   const char* kind = t.variant == kVariantTc ? "tc" : (t.variant == kVariantSk ? "sk" : "mma");
   const char last = t.variant != kVariantSk ? 'c' : (t.mode == 1 ? 'p' : 'g');
-  snprintf(b, sizeof b, "%s:r%d:t%d:b%d:s%d:%c%d", kind, t.rows, t.tok, t.nbox, t.stages, last,
-           t.cl);
+  char lt[16] = "";
+  if (t.lt > 0) snprintf(lt, sizeof lt, ":d%d", t.lt);
+  snprintf(b, sizeof b, "%s:r%d:t%d:b%d:s%d:%c%d%s", kind, t.rows, t.tok, t.nbox, t.stages, last,
+           t.cl, lt);
   return b;
 }
 
@@ -122,9 +126,18 @@ bool tactic_parse(const char* s, Tactic* t) {
   char kind[16] = {0};
   char last = 0;
   Tactic x;
-  if (s == nullptr || sscanf(s, "%15[^:]:r%d:t%d:b%d:s%d:%c%d", kind, &x.rows, &x.tok, &x.nbox,
-                             &x.stages, &last, &x.cl) != 7)
+  int used = 0;
+  if (s == nullptr || sscanf(s, "%15[^:]:r%d:t%d:b%d:s%d:%c%d%n", kind, &x.rows, &x.tok, &x.nbox,
+                             &x.stages, &last, &x.cl, &used) != 7)
     return false;
+  const char* rest = s + used;
+  if (strncmp(rest, ":d", 2) == 0) {
+    int k = 0, n2 = 0;
+    if (sscanf(rest, ":d%d%n", &k, &n2) != 1 || k < 1 || k > 64) return false;
+    x.lt = k;
+    rest += n2;
+  }
+  if (*rest != '\0') return false;
   if (strcmp(kind, "tc") == 0 && last == 'c')
     x.variant = kVariantTc;
   else if (strcmp(kind, "mma") == 0 && last == 'c')
@@ -134,6 +147,7 @@ bool tactic_parse(const char* s, Tactic* t) {
     x.mode = last == 'p' ? 1 : 0;
   } else
     return false;
+  if (x.lt && x.variant == kVariantSk) return false;
   *t = x;
   return true;
 }
@@ -361,6 +375,7 @@ int launch_tactic(skinny_gemm_plan* h, const Tactic& t, const void* x, int64_t l
   p.counters = h->counters;
   p.residual = residual;
   p.ldr = ldr;
+  p.pdl_late = t.lt;
   if (h->debug_count > 0) {
     --h->debug_count;
     p.debug_wait = 1;
@@ -441,6 +456,15 @@ int active_clusters(const skinny_gemm_plan* h, const Tactic& t) {
   return n;
 }
 
+// Number of refill stages of a CTA's K range after its first `stages` (the
+// late-trigger settings 1..span launch dependents at distinct points).
+int late_trigger_span(const skinny_gemm_plan* h, const Tactic& t) {
+  if (t.variant == kVariantSk || t.cl < 1) return 0;
+  const int nb = static_cast<int>((h->kboxes + t.cl - 1) / t.cl);
+  const int iters = (nb + t.nbox - 1) / t.nbox;
+  return std::max(0, iters - std::min(iters, t.stages));
+}
+
 // Candidate tactics for M: the smallest token tile >= M of each variant,
 // every stage count / box count / cluster size that fits and can launch.
 std::vector<Tactic> candidates(const skinny_gemm_plan* h, int64_t M) {
@@ -507,6 +531,9 @@ Tactic default_tactic(const skinny_gemm_plan* h, int64_t M) {
     t.cl = cl;
     const int iters = ((h->kboxes + cl - 1) / cl + t.nbox - 1) / t.nbox;
     t.stages = std::max(1, std::min(t.stages, iters));
+    // Late PDL trigger (measured on the 3584x7168 and 6288x7168 weights): with
+    // 2 (tcgen05) or 3 (mma.sync) stages still to issue.
+    t.lt = t.variant == kVariantMma ? 3 : 2;
     for (; t.stages >= 1; --t.stages)
       if (tactic_fits(h, t, M, nullptr)) return t;
     return Tactic{};
@@ -1079,12 +1106,10 @@ int skinny_gemm_autotune(skinny_gemm_t h, const int64_t* Ms, int nM, void* strea
   std::vector<int64_t> tuned;
   for (int i = 0; i < nM && rc == SKG_OK; ++i) {
     const int64_t M = Ms[i];
-    std::vector<Tactic> cand = candidates(h, M);
-    double best_us = 1e30;
-    Tactic best;
-    for (const Tactic& t : cand) {
-      rc = ensure_workspace(h, t);
-      if (rc != SKG_OK) break;
+    // Time one tactic as a graph of L back-to-back launches over the rotated copies.
+    auto time_tactic = [&](const Tactic& t, double* us_out) -> int {
+      int trc = ensure_workspace(h, t);
+      if (trc != SKG_OK) return trc;
       for (skinny_gemm_plan& sh : shadow) {
         sh.workspace = h->workspace;
         sh.workspace_bytes = h->workspace_bytes;
@@ -1093,54 +1118,74 @@ int skinny_gemm_autotune(skinny_gemm_t h, const int64_t* Ms, int nM, void* strea
       }
       cudaGraph_t graph = nullptr;
       cudaGraphExec_t exec = nullptr;
-      e = cudaStreamBeginCapture(ts, cudaStreamCaptureModeThreadLocal);
-      if (e != cudaSuccess) {
-        rc = cuda_fail(e, "cudaStreamBeginCapture(autotune)");
-        break;
-      }
-      for (int l = 0; l < L && rc == SKG_OK; ++l)
-        rc = launch_tactic(&shadow[l % R], t, xbuf, h->K, M, obuf, h->N, ts);
-      e = cudaStreamEndCapture(ts, &graph);
-      if (rc != SKG_OK || e != cudaSuccess) {
+      cudaError_t ce = cudaStreamBeginCapture(ts, cudaStreamCaptureModeThreadLocal);
+      if (ce != cudaSuccess) return cuda_fail(ce, "cudaStreamBeginCapture(autotune)");
+      for (int l = 0; l < L && trc == SKG_OK; ++l)
+        trc = launch_tactic(&shadow[l % R], t, xbuf, h->K, M, obuf, h->N, ts);
+      ce = cudaStreamEndCapture(ts, &graph);
+      if (trc != SKG_OK || ce != cudaSuccess) {
         if (graph) cudaGraphDestroy(graph);
-        if (rc == SKG_OK) rc = cuda_fail(e, "cudaStreamEndCapture(autotune)");
-        break;
+        return trc != SKG_OK ? trc : cuda_fail(ce, "cudaStreamEndCapture(autotune)");
       }
-      e = cudaGraphInstantiate(&exec, graph, 0);
-      if (e != cudaSuccess) {
+      ce = cudaGraphInstantiate(&exec, graph, 0);
+      if (ce != cudaSuccess) {
         cudaGraphDestroy(graph);
-        rc = cuda_fail(e, "cudaGraphInstantiate(autotune)");
-        break;
+        return cuda_fail(ce, "cudaGraphInstantiate(autotune)");
       }
       float best_ms = 1e30f;
-      e = cudaGraphLaunch(exec, ts);  // warm-up
-      for (int r = 0; r < reps && e == cudaSuccess; ++r) {
+      ce = cudaGraphLaunch(exec, ts);  // warm-up
+      for (int r = 0; r < reps && ce == cudaSuccess; ++r) {
         cudaEventRecord(e0, ts);
-        e = cudaGraphLaunch(exec, ts);
+        ce = cudaGraphLaunch(exec, ts);
         cudaEventRecord(e1, ts);
-        if (e == cudaSuccess) e = cudaEventSynchronize(e1);
+        if (ce == cudaSuccess) ce = cudaEventSynchronize(e1);
         float ms = 0;
-        if (e == cudaSuccess) {
+        if (ce == cudaSuccess) {
           cudaEventElapsedTime(&ms, e0, e1);
           best_ms = std::min(best_ms, ms);
         }
       }
       cudaGraphExecDestroy(exec);
       cudaGraphDestroy(graph);
-      if (e != cudaSuccess) {
-        rc = cuda_fail(e, "autotune timing");
-        break;
-      }
-      const double us = 1000.0 * best_ms / L;
+      if (ce != cudaSuccess) return cuda_fail(ce, "autotune timing");
+      *us_out = 1000.0 * best_ms / L;
       if (log_enabled())
         fprintf(stderr, "[skinny_gemm] tune N=%lld K=%lld M=%lld %s %.3f us\n",
                 static_cast<long long>(h->N), static_cast<long long>(h->K),
-                static_cast<long long>(M), tactic_str(t).c_str(), us);
-      if (us < best_us) {
-        best_us = us;
-        best = t;
+                static_cast<long long>(M), tactic_str(t).c_str(), *us_out);
+      return SKG_OK;
+    };
+    // Phase 1: every candidate with the PDL trigger right after the first stages.
+    std::vector<std::pair<double, Tactic>> timed;
+    for (const Tactic& t : candidates(h, M)) {
+      double us = 0;
+      rc = time_tactic(t, &us);
+      if (rc != SKG_OK) break;
+      timed.push_back({us, t});
+    }
+    // Phase 2: the fastest few again with later PDL triggers.
+    if (rc == SKG_OK) {
+      std::stable_sort(timed.begin(), timed.end(),
+                       [](const auto& a, const auto& b) { return a.first < b.first; });
+      const size_t top = std::min<size_t>(timed.size(), 3);
+      for (size_t c = 0; c < top && rc == SKG_OK; ++c) {
+        for (int lt = 1; lt <= 4 && rc == SKG_OK; ++lt) {
+          Tactic t = timed[c].second;
+          if (t.variant == kVariantSk || late_trigger_span(h, t) < lt) break;
+          t.lt = lt;
+          double us = 0;
+          rc = time_tactic(t, &us);
+          if (rc == SKG_OK) timed.push_back({us, t});
+        }
       }
     }
+    double best_us = 1e30;
+    Tactic best;
+    for (const auto& ut : timed)
+      if (ut.first < best_us) {
+        best_us = ut.first;
+        best = ut.second;
+      }
     if (rc == SKG_OK && best.valid()) {
       h->plan[M] = best;
       tuned.push_back(M);

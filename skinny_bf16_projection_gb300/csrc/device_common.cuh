@@ -177,6 +177,21 @@ __device__ __forceinline__ void cluster_arrive_release() {
 __device__ __forceinline__ void cluster_wait_acquire() {
   asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
 }
+// Shared-memory writes by this thread become visible to the async proxy (bulk copies).
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory into a
+// peer CTA's shared memory, counted on the peer's mbarrier (both addresses
+// already mapped into the cluster window with mapa).
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src_cta,
+                                                  uint32_t bytes, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst_cluster),
+      "r"(src_cta), "r"(bytes), "r"(bar_cluster)
+      : "memory");
+}
 // Address of the same shared-memory variable in CTA `rank` of this cluster.
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   uint32_t r;
@@ -228,6 +243,76 @@ __device__ __forceinline__ void store_out(const KParams& p, int t, int n, float 
   if (p.residual != nullptr)
     v += from_out(static_cast<const OutT*>(p.residual)[static_cast<int64_t>(t) * p.ldr + n]);
   static_cast<OutT*>(p.out)[static_cast<int64_t>(t) * p.ldo + n] = to_out<OutT>(v);
+}
+
+// Two 2-byte output values packed into / unpacked from one 32-bit word (low half first).
+template <typename OutT>
+__device__ __forceinline__ uint32_t pack2(float a, float b);
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float a, float b) {
+  const __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+template <typename OutT>
+__device__ __forceinline__ float2 unpack2(uint32_t u);
+template <>
+__device__ __forceinline__ float2 unpack2<__nv_bfloat16>(uint32_t u) {
+  return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+template <>
+__device__ __forceinline__ float2 unpack2<__half>(uint32_t u) {
+  __half2 h;
+  *reinterpret_cast<uint32_t*>(&h) = u;
+  return __half22float2(h);
+}
+
+// Eight consecutive outputs out[t][n..n+7] with one (bf16/fp16) or two (fp32)
+// 16-byte stores; same arithmetic as store_out per element.  The caller checks
+// that out (and residual) rows are 16-byte aligned at n and n + 8 <= N.
+template <typename OutT>
+__device__ __forceinline__ void store_out8(const KParams& p, int t, int n, const float (&v)[8]) {
+  float w[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) w[j] = v[j];
+  if (p.residual != nullptr) {
+    const OutT* rp = static_cast<const OutT*>(p.residual) + static_cast<int64_t>(t) * p.ldr + n;
+    if constexpr (sizeof(OutT) == 2) {
+      const uint4 q = *reinterpret_cast<const uint4*>(rp);
+      const float2 a = unpack2<OutT>(q.x), b = unpack2<OutT>(q.y), c = unpack2<OutT>(q.z),
+                   d = unpack2<OutT>(q.w);
+      w[0] += a.x; w[1] += a.y; w[2] += b.x; w[3] += b.y;
+      w[4] += c.x; w[5] += c.y; w[6] += d.x; w[7] += d.y;
+    } else {
+      const float4 a = *reinterpret_cast<const float4*>(rp);
+      const float4 b = *reinterpret_cast<const float4*>(rp + 4);
+      w[0] += a.x; w[1] += a.y; w[2] += a.z; w[3] += a.w;
+      w[4] += b.x; w[5] += b.y; w[6] += b.z; w[7] += b.w;
+    }
+  }
+  OutT* op = static_cast<OutT*>(p.out) + static_cast<int64_t>(t) * p.ldo + n;
+  if constexpr (sizeof(OutT) == 2) {
+    *reinterpret_cast<uint4*>(op) = make_uint4(pack2<OutT>(w[0], w[1]), pack2<OutT>(w[2], w[3]),
+                                               pack2<OutT>(w[4], w[5]), pack2<OutT>(w[6], w[7]));
+  } else {
+    *reinterpret_cast<float4*>(op) = make_float4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<float4*>(op + 4) = make_float4(w[4], w[5], w[6], w[7]);
+  }
+}
+
+// True when every row of out (and of residual, if any) starts 16-byte aligned
+// for 8-element column blocks, so store_out8 may be used at n % 8 == 0.
+template <typename OutT>
+__device__ __forceinline__ bool rows_vectorizable(const KParams& p) {
+  constexpr int64_t e = static_cast<int64_t>(sizeof(OutT));
+  bool ok = (reinterpret_cast<uintptr_t>(p.out) % 16 == 0) && ((p.ldo * e) % 16 == 0);
+  if (p.residual != nullptr)
+    ok = ok && (reinterpret_cast<uintptr_t>(p.residual) % 16 == 0) && ((p.ldr * e) % 16 == 0);
+  return ok;
 }
 
 // ---------------------------------------------------------------- mma.sync (legacy path)

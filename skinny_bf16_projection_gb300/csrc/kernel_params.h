@@ -30,7 +30,8 @@ struct KParams {
   uint32_t* status;       // device status word (watchdog)
   uint64_t timeout_ns;    // bound of every spin wait
   int32_t debug_wait;     // nonzero: watchdog self-test, wait on a dead barrier and return
-  int32_t pad_;
+  int32_t pdl_late;       // 0: launch dependents right after the first stages' weight loads;
+                          // k >= 1: only once all but the last k-1 stages' loads are issued
   // stream-K kernel only: fp32 partial sums of split tiles and per-tile arrival counters
   float* workspace;       // [gridDim.x][2][TOK][128]
   uint32_t* counters;     // [ceil(N / 128)], zero between launches

@@ -106,10 +106,14 @@ __global__ void __launch_bounds__(160) skinny_mma_kernel(const __grid_constant__
           tma_load_2d_hint(st + b * kWBox, &wmap, (kb0 + it * NBOX + b) * kBoxK, n0, full_bar(it),
                            policy);
       }
-      // Let the next kernel on the stream launch now: its CTAs can prefetch their
-      // own weight tiles while this grid streams (they still wait for our
-      // completion in griddepcontrol.wait before touching x or out).
-      pdl_launch_dependents();
+      // Let the next kernel on the stream launch: its CTAs prefetch their own
+      // weight tiles into whatever shared memory is free (they still wait for
+      // our completion in griddepcontrol.wait before touching x or out).  By
+      // default that happens now; with pdl_late it waits until this CTA has
+      // issued (nearly) all of its weight loads, so the next grid's first
+      // loads queue up behind ours instead of competing with them.
+      const int trig = p.pdl_late > 0 ? max(pro, iters - p.pdl_late + 1) : pro;
+      if (trig == pro) pdl_launch_dependents();
       pdl_wait();
       for (int it = 0; it < pro; ++it) {
         const int nbi = min(NBOX, nb - it * NBOX);
@@ -118,6 +122,7 @@ __global__ void __launch_bounds__(160) skinny_mma_kernel(const __grid_constant__
           tma_load_2d(st + b * kXBox, &xmap, (kb0 + it * NBOX + b) * kBoxK, 0, full_bar(it));
       }
       for (int it = pro; it < iters; ++it) {
+        if (it == trig) pdl_launch_dependents();
         const int s = it % S;
         const uint32_t ph = static_cast<uint32_t>((it / S) - 1) & 1u;
         if (!mbar_wait_bounded(empty_bar(s), ph, p.timeout_ns))
@@ -132,6 +137,7 @@ __global__ void __launch_bounds__(160) skinny_mma_kernel(const __grid_constant__
           tma_load_2d(st + NBOX * kWBox + b * kXBox, &xmap, (kb0 + it * NBOX + b) * kBoxK, 0,
                       full_bar(s));
       }
+      if (trig == iters && trig != pro) pdl_launch_dependents();
     }
     __syncwarp();
   } else {

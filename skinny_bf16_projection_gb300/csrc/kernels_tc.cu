@@ -40,6 +40,7 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
   constexpr uint32_t kStage = stage_bytes(ROWS, TOK, NBOX);
   constexpr uint32_t kTmemCols = TOK <= 32 ? 32u : static_cast<uint32_t>(TOK);
   constexpr uint32_t kIdesc = mma_idesc<kFp16>(ROWS, TOK);
+  constexpr uint32_t kStageRed = static_cast<uint32_t>(ROWS * TOK) * 4u;
   static_assert(TOK % 16 == 0 && TOK >= 16 && TOK <= 256, "M=128 MMA needs N % 16 == 0, N <= 256");
 
   extern __shared__ uint8_t smem_raw[];
@@ -81,6 +82,11 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
   const int iters = (nb + NBOX - 1) / NBOX;
   const int RS = ROWS / static_cast<int>(csize);
   const int M = p.M;
+  // Cluster reduction: for token tiles of 64 and more, bulk DSMEM copies of
+  // [TOK][RS] fp32 blocks staged in the idle pipeline buffers (when they are
+  // large enough); for smaller tiles per-thread st.async pushes, which measured
+  // faster there.
+  const bool bulk = csize > 1 && TOK >= 64 && static_cast<uint32_t>(S) * kStage >= kStageRed;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -89,7 +95,9 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
     }
     mbar_init(done_bar, 1);
     mbar_init(recv_bar, 1);
-    if (csize > 1) mbar_arrive_expect_tx(recv_bar, (csize - 1) * RS * ((M + 3) / 4) * 16u);
+    if (csize > 1)
+      mbar_arrive_expect_tx(recv_bar, bulk ? (csize - 1) * static_cast<uint32_t>(M * RS) * 4u
+                                           : (csize - 1) * RS * ((M + 3) / 4) * 16u);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -116,10 +124,14 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
           tma_load_2d_hint(st + b * kWBox, &wmap, (kb0 + it * NBOX + b) * kBoxK, n0, full_bar(it),
                            policy);
       }
-      // Let the next kernel on the stream launch now: its CTAs can prefetch their
-      // own weight tiles while this grid streams (they still wait for our
-      // completion in griddepcontrol.wait before touching x or out).
-      pdl_launch_dependents();
+      // Let the next kernel on the stream launch: its CTAs prefetch their own
+      // weight tiles into whatever shared memory is free (they still wait for
+      // our completion in griddepcontrol.wait before touching x or out).  By
+      // default that happens now; with pdl_late it waits until this CTA has
+      // issued (nearly) all of its weight loads, so the next grid's first
+      // loads queue up behind ours instead of competing with them.
+      const int trig = p.pdl_late > 0 ? max(pro, iters - p.pdl_late + 1) : pro;
+      if (trig == pro) pdl_launch_dependents();
       pdl_wait();  // x is produced by the previous kernel on the stream
       for (int it = 0; it < pro; ++it) {
         const int nbi = min(NBOX, nb - it * NBOX);
@@ -128,6 +140,7 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
           tma_load_2d(st + b * kXBox, &xmap, (kb0 + it * NBOX + b) * kBoxK, 0, full_bar(it));
       }
       for (int it = pro; it < iters; ++it) {
+        if (it == trig) pdl_launch_dependents();
         const int s = it % S;
         const uint32_t ph = static_cast<uint32_t>((it / S) - 1) & 1u;
         if (!mbar_wait_bounded(empty_bar(s), ph, p.timeout_ns))
@@ -142,6 +155,7 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
           tma_load_2d(st + NBOX * kWBox + b * kXBox, &xmap, (kb0 + it * NBOX + b) * kBoxK, 0,
                       full_bar(s));
       }
+      if (trig == iters && trig != pro) pdl_launch_dependents();
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -201,6 +215,76 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
           if (c0 + i < M) store_out<OutT>(p, c0 + i, n, v[i]);
       }
     }
+  } else if (bulk) {
+    cluster_wait_acquire();  // every peer's receive barrier is initialised
+    // Token-major blocks [owner][TOK][RS]: each row's partial sums go to the
+    // block of the CTA that owns the row, staged in this CTA's idle pipeline
+    // buffers (every TMA load has landed and every MMA has read its operands
+    // once done_bar fired); the own block is written straight into `red`,
+    // which receives the peers' blocks in the same layout at [rank].
+    const uint32_t blk = static_cast<uint32_t>(TOK * RS) * 4u;
+    const uint32_t owner = static_cast<uint32_t>(r / RS);
+    const uint32_t dst = (owner == rank ? red : base) + owner * blk + static_cast<uint32_t>(r % RS) * 4u;
+    for (int c0 = 0; c0 < TOK && c0 < M; c0 += CH) {
+      float v[CH];
+      load_chunk(c0, v);
+#pragma unroll
+      for (int i = 0; i < CH; ++i)
+        if (c0 + i < M)
+          asm volatile("st.shared.f32 [%0], %1;" ::"r"(dst + static_cast<uint32_t>((c0 + i) * RS) * 4u),
+                       "f"(v[i])
+                       : "memory");
+    }
+    fence_proxy_async_shared();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const uint32_t bytes = static_cast<uint32_t>(M * RS) * 4u;
+      for (uint32_t j = 1; j < csize; ++j) {
+        const uint32_t o = (rank + j) % csize;
+        bulk_copy_to_peer(mapa_shared(red + rank * blk, o), base + o * blk, bytes,
+                          mapa_shared(recv_bar, o));
+      }
+    }
+    if (!mbar_wait_bounded<true>(recv_bar, 0, p.timeout_ns))
+      report_status(p.status, kStatusTimeoutRecv);
+    // Once every CTA of the cluster has received its blocks, no copy still reads
+    // this CTA's staging buffers: arrive now, wait before exiting.
+    cluster_arrive_release();
+    // Reduce in rank order (deterministic) 8 rows x 1 token per step and store
+    // the 8 outputs, contiguous in out[t], with 16-byte stores where aligned.
+    const int RB = RS / 8;
+    const int nbase = n0 + static_cast<int>(rank) * RS;
+    const bool vec = rows_vectorizable<OutT>(p);
+    for (int idx = threadIdx.x; idx < M * RB; idx += blockDim.x) {
+      const int t = idx / RB;
+      const int rb = idx % RB;
+      float acc[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+      for (uint32_t k = 0; k < csize; ++k) {
+        const uint32_t a = red + k * blk + static_cast<uint32_t>(t * RS + rb * 8) * 4u;
+        float4 q0, q1;
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(q0.x), "=f"(q0.y), "=f"(q0.z), "=f"(q0.w)
+                     : "r"(a)
+                     : "memory");
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(q1.x), "=f"(q1.y), "=f"(q1.z), "=f"(q1.w)
+                     : "r"(a + 16u)
+                     : "memory");
+        acc[0] += q0.x; acc[1] += q0.y; acc[2] += q0.z; acc[3] += q0.w;
+        acc[4] += q1.x; acc[5] += q1.y; acc[6] += q1.z; acc[7] += q1.w;
+      }
+      const int n = nbase + rb * 8;
+      if (vec && n + 8 <= p.N) {
+        store_out8<OutT>(p, t, n, acc);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (n + j < p.N) store_out<OutT>(p, t, n + j, acc[j]);
+      }
+    }
+    cluster_wait_acquire();
   } else {
     cluster_wait_acquire();  // every peer's receive barrier is initialised
     // Receive buffer [rank][RS][TP]: each row's tokens contiguous (16-byte pushes),
@@ -231,28 +315,29 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
     __syncthreads();
     if (!mbar_wait_bounded<true>(recv_bar, 0, p.timeout_ns))
       report_status(p.status, kStatusTimeoutRecv);
+    // Reduce in rank order (deterministic) 8 rows x 1 token per step (lanes
+    // walk the token index: conflict-free reads) and store the 8 outputs,
+    // contiguous in out[t], with 16-byte stores where aligned.
+    const int RB = RS / 8;
     const int nbase = n0 + static_cast<int>(rank) * RS;
-    for (int idx = threadIdx.x; idx < RS * MG; idx += blockDim.x) {
-      const int rs2 = idx % RS;
-      const int g = idx / RS;
-      float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-      for (uint32_t k = 0; k < csize; ++k) {
-        float4 q;
-        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                     : "=f"(q.x), "=f"(q.y), "=f"(q.z), "=f"(q.w)
-                     : "r"(red + ((k * RS + rs2) * TP + 4 * g) * 4u)
-                     : "memory");
-        acc.x += q.x;
-        acc.y += q.y;
-        acc.z += q.z;
-        acc.w += q.w;
-      }
-      const int n = nbase + rs2;
-      if (n < p.N) {
-        store_out<OutT>(p, 4 * g, n, acc.x);
-        if (4 * g + 1 < M) store_out<OutT>(p, 4 * g + 1, n, acc.y);
-        if (4 * g + 2 < M) store_out<OutT>(p, 4 * g + 2, n, acc.z);
-        if (4 * g + 3 < M) store_out<OutT>(p, 4 * g + 3, n, acc.w);
+    const bool vec = rows_vectorizable<OutT>(p);
+    const float* redf = reinterpret_cast<const float*>(gbase + (red - base));
+    for (int idx = threadIdx.x; idx < M * RB; idx += blockDim.x) {
+      const int t = idx % M;
+      const int rb = idx / M;
+      float acc[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+      for (uint32_t k = 0; k < csize; ++k)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] += redf[(k * RS + rb * 8 + j) * TP + t];
+      const int n = nbase + rb * 8;
+      if (vec && n + 8 <= p.N) {
+        store_out8<OutT>(p, t, n, acc);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (n + j < p.N) store_out<OutT>(p, t, n + j, acc[j]);
       }
     }
   }

@@ -348,3 +348,51 @@ def test_dependent_chain_without_pdl_matches_with_pdl():
         results.append(bufs[-1].clone())
         proj.close()
     assert torch.equal(results[0], results[1])
+
+
+def test_late_pdl_trigger_chain_matches_no_pdl():
+    """Launching the dependent grid later (tactic suffix ":d<k>": only once all
+    but k-1 stages' weight loads are issued) changes when the next launch's
+    weight prologue starts, never what it reads: a dependent chain with every
+    trigger setting, eager and as one CUDA graph, gives the bits of the same
+    tactic launched without programmatic dependent launch."""
+    D = 4096
+    w = pin.weight(D, D, seed=11, std=1.0 / np.sqrt(D))
+    wd = w.to(DEV)
+    x0 = pin.case(8, D, seed=12, max_tokens=32)[1]
+    with_pdl = skg().Projection(wd, use_tactic_file=False)
+    no_pdl = skg().Projection(wd, use_tactic_file=False, pdl=False)
+    links = 6
+    for M in (1, 16, 32):
+        bases = [t for t in with_pdl.tactics(M) if not t.startswith("sk")][::5]
+        for base in bases:
+            no_pdl.set_tactic(M, base)
+            ref = [x0[:M].to(DEV)] + [torch.empty((M, D), dtype=torch.bfloat16, device=DEV)
+                                      for _ in range(links)]
+            for i in range(links):
+                no_pdl.run(ref[i], ref[i + 1])
+            torch.cuda.synchronize()
+            for k in (1, 2, 3, 4):
+                with_pdl.set_tactic(M, f"{base}:d{k}")
+                assert with_pdl.plan(M) == f"{base}:d{k}"
+                bufs = [ref[0]] + [torch.full((M, D), float("nan"), dtype=torch.bfloat16,
+                                              device=DEV) for _ in range(links)]
+                for i in range(links):
+                    with_pdl.run(bufs[i], bufs[i + 1])
+                torch.cuda.synchronize()
+                assert torch.equal(bufs[-1], ref[-1]), f"eager {base}:d{k} M={M}"
+                for b in bufs[1:]:
+                    b.fill_(float("nan"))
+                side = torch.cuda.Stream()
+                side.wait_stream(torch.cuda.current_stream())
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=side):
+                    for i in range(links):
+                        with_pdl.run(bufs[i], bufs[i + 1])
+                g.replay()
+                torch.cuda.synchronize()
+                assert torch.equal(bufs[-1], ref[-1]), f"graph {base}:d{k} M={M}"
+    ref_s, s_s = oracle.projection(ref[0].cpu(), w)
+    assert_parity(ref[1], ref_s, s_s, "first link")
+    with_pdl.close()
+    no_pdl.close()
