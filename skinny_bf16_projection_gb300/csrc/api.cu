@@ -299,7 +299,9 @@ bool tactic_fits(const skinny_gemm_plan* h, const Tactic& t, int64_t M, std::str
   if (!t.valid()) return no("empty tactic");
   const KernelEntry* k = find_kernel(t, h->dtype, h->out_dtype);
   if (k == nullptr) return no("no compiled kernel for this rows/tok/box/dtype combination");
-  if (M > t.tok) return no("token tile smaller than M");
+  // tcgen05 tactics cover M > tok with ceil(M / tok) token tiles (grid y);
+  // the others need one tile of at least M tokens.
+  if (M > t.tok && t.variant != kVariantTc) return no("token tile smaller than M");
   if (t.variant == kVariantSk) {
     if (t.mode == 0 && t.cl != 1 && t.cl != 2) return no("stream-K runs 1 or 2 CTAs per SM");
     if (t.mode == 1 && (t.cl < 1 || t.cl > 64 || t.cl > h->kboxes))
@@ -382,7 +384,8 @@ int launch_tactic(skinny_gemm_plan* h, const Tactic& t, const void* x, int64_t l
     p.timeout_ns = h->debug_timeout_ns;
   }
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(static_cast<unsigned>(tactic_grid(h, t)), 1, 1);
+  const unsigned ty = t.variant == kVariantTc ? static_cast<unsigned>((M + t.tok - 1) / t.tok) : 1u;
+  cfg.gridDim = dim3(static_cast<unsigned>(tactic_grid(h, t)), ty, 1);
   cfg.blockDim = dim3(static_cast<unsigned>(k->threads), 1, 1);
   cfg.dynamicSmemBytes = tactic_smem(t);
   cfg.stream = st;
@@ -432,7 +435,7 @@ int active_clusters(const skinny_gemm_plan* h, const Tactic& t) {
     per_sm = std::min(per_sm, regs > 0 ? d.regs_per_sm / regs : per_sm);
     per_sm = std::min(per_sm, d.smem_per_sm / static_cast<int>(tactic_smem(t) + d.smem_reserved));
     const int tmem_cols = t.variant == kVariantSk  ? (2 * t.tok <= 32 ? 32 : (2 * t.tok <= 64 ? 64 : 128))
-                          : t.variant == kVariantTc ? (t.tok <= 32 ? 32 : 64)
+                          : t.variant == kVariantTc ? std::max(32, t.tok)
                                                     : 0;
     if (tmem_cols > 0) per_sm = std::min(per_sm, 512 / tmem_cols);
     return std::max(per_sm, 0) * d.sm_count;
@@ -465,20 +468,26 @@ int late_trigger_span(const skinny_gemm_plan* h, const Tactic& t) {
   return std::max(0, iters - std::min(iters, t.stages));
 }
 
-// Candidate tactics for M: the smallest token tile >= M of each variant,
-// every stage count / box count / cluster size that fits and can launch.
+// Candidate tactics for M: the smallest token tile >= M of each variant (for
+// M > 64 also tcgen05 tiles of 64 and 128 tokens repeated over ceil(M / tok)
+// token tiles), every stage count / box count / cluster size that fits and
+// can launch.
 std::vector<Tactic> candidates(const skinny_gemm_plan* h, int64_t M) {
   std::vector<Tactic> out;
+  std::vector<std::pair<int, int>> vt;  // (variant, token tile)
   for (int variant : {kVariantTc, kVariantMma, kVariantSk}) {
     const int* toks = variant == kVariantMma ? kMmaToks : kTcToks;
     const int ntok = variant == kVariantMma ? 3 : (variant == kVariantSk ? 3 : 5);
-    int tok = 0;
     for (int i = 0; i < ntok; ++i)
       if (toks[i] >= M) {
-        tok = toks[i];
+        vt.push_back({variant, toks[i]});
         break;
       }
-    if (tok == 0) continue;
+    if (variant == kVariantTc && M > 64)
+      for (int tok : {64, 128})
+        if (tok < M) vt.push_back({variant, tok});
+  }
+  for (const auto& [variant, tok] : vt) {
     for (const KernelEntry* k : all_kernels()) {
       if (k->variant != variant || k->tok != tok || k->in_dtype != h->dtype ||
           k->out_dtype != h->out_dtype)
@@ -516,17 +525,21 @@ std::vector<Tactic> candidates(const skinny_gemm_plan* h, int64_t M) {
 //   M <= 16  mma.sync, 64-row tiles, 16-token tile, 2 boxes x 2 stages
 //   M <= 32  tcgen05, 32-token tile, 2 boxes x 2 stages
 //   M <= 64  tcgen05, 64-token tile, 1 box x 3 stages
-// with the cluster split (split-K factor) that gives about 1.4 CTAs per SM,
-// at most 8; fewer stages where shared memory or the K range is short.  Any
+// with the cluster split (split-K factor) that gives about 1.4 CTAs per SM
+// (64-row tiles: at most 3), at most 8; fewer stages where shared memory or
+// the K range is short.  Any
 // choice that does not fit falls back to fewer stages, then to the tcgen05
 // kernel with the same rule.
 Tactic default_tactic(const skinny_gemm_plan* h, int64_t M) {
   Tactic best;
-  auto with_cluster = [&](Tactic t) {
+  // Split-K cluster size: the smallest giving at least 1.4 CTAs per SM, or
+  // (cap3, the 64-row tiles) the largest giving at most 3 CTAs per SM.
+  auto with_cluster = [&](Tactic t, bool cap3 = false) {
     const int ntiles = static_cast<int>((h->N + t.rows - 1) / t.rows);
+    const int sms = h->dev->sm_count;
     int cl = 1;
-    while (cl < 8 && ntiles * cl * 10 < h->dev->sm_count * 14 && cl * 2 <= h->kboxes &&
-           t.rows % (cl * 2) == 0)
+    while (cl < 8 && cl * 2 <= h->kboxes && t.rows % (cl * 2) == 0 &&
+           (cap3 ? ntiles * cl * 2 <= 3 * sms : ntiles * cl * 10 < sms * 14))
       cl *= 2;
     t.cl = cl;
     const int iters = ((h->kboxes + cl - 1) / cl + t.nbox - 1) / t.nbox;
@@ -542,7 +555,7 @@ Tactic default_tactic(const skinny_gemm_plan* h, int64_t M) {
   if (M <= 8)
     t = with_cluster(Tactic{kVariantMma, 128, 8, 2, 3, 1, 0});
   else if (M <= 16)
-    t = with_cluster(Tactic{kVariantMma, 64, 16, 2, 2, 1, 0});
+    t = with_cluster(Tactic{kVariantMma, 64, 16, 2, 2, 1, 0}, true);
   else if (M <= 32)
     t = with_cluster(Tactic{kVariantTc, 128, 32, 2, 2, 1, 0});
   else if (M <= 64)

@@ -81,7 +81,10 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
   const int nb = kb1 - kb0;
   const int iters = (nb + NBOX - 1) / NBOX;
   const int RS = ROWS / static_cast<int>(csize);
-  const int M = p.M;
+  // Token tile of this CTA (gridDim.y > 1 when M exceeds the tile): rows
+  // m0 .. m0 + M - 1 of x and out.
+  const int m0 = static_cast<int>(blockIdx.y) * TOK;
+  const int M = min(TOK, p.M - m0);
   // Cluster reduction: for token tiles of 64 and more, bulk DSMEM copies of
   // [TOK][RS] fp32 blocks staged in the idle pipeline buffers (when they are
   // large enough); for smaller tiles per-thread st.async pushes, which measured
@@ -114,7 +117,9 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
     if (lane == 0) {
       prefetch_tensormap(&wmap);
       prefetch_tensormap(&xmap);
-      const uint64_t policy = l2_policy_evict_first();
+      // Weight tiles are streamed once (evict first), unless other token tiles'
+      // CTAs read the same tiles again (then keep them at normal priority).
+      const uint64_t policy = gridDim.y > 1 ? l2_policy_evict_normal() : l2_policy_evict_first();
       const int pro = iters < S ? iters : S;
       for (int it = 0; it < pro; ++it) {
         const int nbi = min(NBOX, nb - it * NBOX);
@@ -137,7 +142,7 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
         const int nbi = min(NBOX, nb - it * NBOX);
         const uint32_t st = base + static_cast<uint32_t>(it) * kStage + NBOX * kWBox;
         for (int b = 0; b < nbi; ++b)
-          tma_load_2d(st + b * kXBox, &xmap, (kb0 + it * NBOX + b) * kBoxK, 0, full_bar(it));
+          tma_load_2d(st + b * kXBox, &xmap, (kb0 + it * NBOX + b) * kBoxK, m0, full_bar(it));
       }
       for (int it = pro; it < iters; ++it) {
         if (it == trig) pdl_launch_dependents();
@@ -152,7 +157,7 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
           tma_load_2d_hint(st + b * kWBox, &wmap, (kb0 + it * NBOX + b) * kBoxK, n0, full_bar(s),
                            policy);
         for (int b = 0; b < nbi; ++b)
-          tma_load_2d(st + NBOX * kWBox + b * kXBox, &xmap, (kb0 + it * NBOX + b) * kBoxK, 0,
+          tma_load_2d(st + NBOX * kWBox + b * kXBox, &xmap, (kb0 + it * NBOX + b) * kBoxK, m0,
                       full_bar(s));
       }
       if (trig == iters && trig != pro) pdl_launch_dependents();
@@ -212,7 +217,7 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
       if (n < p.N) {
 #pragma unroll
         for (int i = 0; i < CH; ++i)
-          if (c0 + i < M) store_out<OutT>(p, c0 + i, n, v[i]);
+          if (c0 + i < M) store_out<OutT>(p, m0 + c0 + i, n, v[i]);
       }
     }
   } else if (bulk) {
@@ -277,11 +282,11 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
       }
       const int n = nbase + rb * 8;
       if (vec && n + 8 <= p.N) {
-        store_out8<OutT>(p, t, n, acc);
+        store_out8<OutT>(p, m0 + t, n, acc);
       } else {
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          if (n + j < p.N) store_out<OutT>(p, t, n + j, acc[j]);
+          if (n + j < p.N) store_out<OutT>(p, m0 + t, n + j, acc[j]);
       }
     }
     cluster_wait_acquire();
@@ -333,11 +338,11 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
         for (int j = 0; j < 8; ++j) acc[j] += redf[(k * RS + rb * 8 + j) * TP + t];
       const int n = nbase + rb * 8;
       if (vec && n + 8 <= p.N) {
-        store_out8<OutT>(p, t, n, acc);
+        store_out8<OutT>(p, m0 + t, n, acc);
       } else {
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          if (n + j < p.N) store_out<OutT>(p, t, n + j, acc[j]);
+          if (n + j < p.N) store_out<OutT>(p, m0 + t, n + j, acc[j]);
       }
     }
   }

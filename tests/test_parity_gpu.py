@@ -280,7 +280,9 @@ def test_error_codes():
     assert lib.skinny_gemm_prepare(w.data_ptr(), 256, 1024, 0, 1) is None
     assert lib.skinny_gemm_last_status() == nat.SKG_EINVAL
     with pytest.raises(m.SkinnyGemmError):
-        proj.set_tactic(40, "tc:r128:t32:b2:s4:c1")  # token tile 32 < M = 40
+        proj.set_tactic(40, "mma:r128:t32:b2:s2:c8")  # mma.sync token tile 32 < M = 40
+    proj.set_tactic(40, "tc:r128:t32:b2:s4:c1")  # tcgen05: two token tiles of 32
+    assert proj.plan(40) == "tc:r128:t32:b2:s4:c1"
     with pytest.raises(m.SkinnyGemmError):
         proj.set_tactic(8, "tc:r128:t16:b2:s4:c32")  # cluster size 32 is not offered
     with pytest.raises(m.SkinnyGemmError):
