@@ -396,6 +396,16 @@ def other_workloads(torch, skg, pin, dev, l2, peak_gbs):
         torch.cuda.empty_cache()
     res["dependent chain: W[3584,7168] -> W[7168,3584] -> ... (each output feeds the next input)"] = \
         dependent_chain(torch, skg, pin, dev, l2, peak_gbs)
+    # Tiny: W[1536,128] (384 KB, L2-resident after the first call: launch-latency bound)
+    wt, xt = pin.case(1536, 128, seed=0)
+    pt = skg.Projection(wt.to(dev))
+    pt.autotune([1])
+    xm = xt[:1].to(dev).contiguous()
+    out = torch.empty((1, 1536), dtype=torch.bfloat16, device=dev)
+    us = graph_time_us(torch, stream, dev, lambda i: pt.run(xm, out), 48)
+    res["tiny: W[1536,128] M=1 (L2-resident, back to back)"] = {"us": round(us, 3),
+                                                                "tactic": pt.plan(1)}
+    pt.close()
     return res
 
 
