@@ -188,14 +188,16 @@ int skinny_gemm_autotune_overlap(skinny_gemm_t h_main, skinny_gemm_t h_fa, skinn
 
 /* Force the tactic used for token count M (1..256), given as the string
  * skinny_gemm_plan_query prints:
- *   "tc:r128:t<tok>:b<boxes>:s<stages>:c<cluster>[:d<k>]"   tcgen05 kernel
+ *   "tc:r128:t<tok>:b<boxes>:s<stages>:c<cluster>[:d<k>][:a]"  tcgen05 kernel
  *   "mma:r<64|128>:t<tok>:b<boxes>:s<stages>:c<cluster>[:d<k>]"  mma.sync kernel
  *   "sk:r128:t<tok>:b<boxes>:s<stages>:<g|p><n>"             stream-K kernel
  * (t = token tile, b = 64-wide K boxes per pipeline stage, c = split-K cluster
  * size, g = CTAs per SM / p = parts per row tile for stream-K; d<k> launches
  * the next kernel on the stream (PDL) only once all but k-1 of a CTA's weight
- * stages are issued).  tcgen05 tactics with tok < M run ceil(M / tok) token
- * tiles; the other kernels need tok >= M.  EINVAL if the string does not
+ * stages are issued; :a places a cluster's receive buffer in the pipeline
+ * stages, which frees shared memory for more CTAs per SM at the price of a
+ * cluster barrier after the MMAs).  tcgen05 tactics with tok < M run
+ * ceil(M / tok) token tiles; the other kernels need tok >= M.  EINVAL if the string does not
  * parse or the tactic does not fit this weight and M. */
 int skinny_gemm_set_tactic(skinny_gemm_t h, int64_t M, const char* tactic);
 

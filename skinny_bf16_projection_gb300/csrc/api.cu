@@ -106,19 +106,21 @@ int encode_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, in
 struct Tactic {
   int variant = 0, rows = 0, tok = 0, nbox = 0, stages = 0, cl = 0, mode = 0;
   int lt = 0;  // k >= 1: launch dependents only with k-1 stages' loads left to issue (mma / tc)
+  int al = 0;  // 1: tcgen05 cluster receive buffer aliases the pipeline stages
   bool valid() const { return variant != 0; }
 };
 
 // "tc:r128:t16:b2:s4:c8" (c = cluster size) or "sk:r128:t16:b2:s5:g1" (g = CTAs per SM),
-// with ":d<k>" appended for a late PDL trigger (mma / tc).
+// with ":d<k>" appended for a late PDL trigger (mma / tc) and ":a" for a tcgen05
+// cluster reduction buffer aliased onto the pipeline stages.
 std::string tactic_str(const Tactic& t) {
   char b[96];
   const char* kind = t.variant == kVariantTc ? "tc" : (t.variant == kVariantSk ? "sk" : "mma");
   const char last = t.variant != kVariantSk ? 'c' : (t.mode == 1 ? 'p' : 'g');
   char lt[16] = "";
   if (t.lt > 0) snprintf(lt, sizeof lt, ":d%d", t.lt);
-  snprintf(b, sizeof b, "%s:r%d:t%d:b%d:s%d:%c%d%s", kind, t.rows, t.tok, t.nbox, t.stages, last,
-           t.cl, lt);
+  snprintf(b, sizeof b, "%s:r%d:t%d:b%d:s%d:%c%d%s%s", kind, t.rows, t.tok, t.nbox, t.stages, last,
+           t.cl, lt, t.al ? ":a" : "");
   return b;
 }
 
@@ -130,14 +132,21 @@ bool tactic_parse(const char* s, Tactic* t) {
   if (s == nullptr || sscanf(s, "%15[^:]:r%d:t%d:b%d:s%d:%c%d%n", kind, &x.rows, &x.tok, &x.nbox,
                              &x.stages, &last, &x.cl, &used) != 7)
     return false;
+  // optional suffixes, in any order, each at most once: ":d<k>", ":a"
   const char* rest = s + used;
-  if (strncmp(rest, ":d", 2) == 0) {
-    int k = 0, n2 = 0;
-    if (sscanf(rest, ":d%d%n", &k, &n2) != 1 || k < 1 || k > 64) return false;
-    x.lt = k;
-    rest += n2;
+  while (*rest != '\0') {
+    if (strncmp(rest, ":d", 2) == 0 && x.lt == 0) {
+      int k = 0, n2 = 0;
+      if (sscanf(rest, ":d%d%n", &k, &n2) != 1 || k < 1 || k > 64) return false;
+      x.lt = k;
+      rest += n2;
+    } else if (strncmp(rest, ":a", 2) == 0 && (rest[2] == '\0' || rest[2] == ':') && x.al == 0) {
+      x.al = 1;
+      rest += 2;
+    } else {
+      return false;
+    }
   }
-  if (*rest != '\0') return false;
   if (strcmp(kind, "tc") == 0 && last == 'c')
     x.variant = kVariantTc;
   else if (strcmp(kind, "mma") == 0 && last == 'c')
@@ -148,6 +157,7 @@ bool tactic_parse(const char* s, Tactic* t) {
   } else
     return false;
   if (x.lt && x.variant == kVariantSk) return false;
+  if (x.al && x.variant != kVariantTc) return false;
   *t = x;
   return true;
 }
@@ -267,7 +277,7 @@ int ntiles_of(const skinny_gemm_plan* h, const Tactic& t) {
 }
 uint32_t tactic_smem(const Tactic& t) {
   if (t.variant == kVariantSk) return sk_smem_bytes(t.tok, t.nbox, t.stages);
-  if (t.variant == kVariantTc) return tc_smem_bytes(t.tok, t.nbox, t.stages, t.cl);
+  if (t.variant == kVariantTc) return tc_smem_bytes(t.tok, t.nbox, t.stages, t.cl, t.al != 0);
   return smem_bytes(t.rows, t.tok, t.nbox, t.stages);
 }
 // CTAs launched: row tiles x cluster size, or (stream-K) CTAs-per-SM x SMs,
@@ -314,6 +324,9 @@ bool tactic_fits(const skinny_gemm_plan* h, const Tactic& t, int64_t M, std::str
     if (t.rows % t.cl != 0) return no("cluster size must divide the row tile");
   }
   if (t.stages < 1 || t.stages > 16) return no("stages out of range 1..16");
+  if (t.al && (t.cl < 2 || static_cast<uint32_t>(t.stages) * stage_bytes(128, t.tok, t.nbox) <
+                               tc_red_bytes(t.tok)))
+    return no("an aliased receive buffer needs a cluster and stages at least as large");
   if (static_cast<int>(tactic_smem(t)) > h->dev->smem_optin)
     return no("shared memory footprint exceeds the per-block limit");
   return true;
@@ -378,6 +391,7 @@ int launch_tactic(skinny_gemm_plan* h, const Tactic& t, const void* x, int64_t l
   p.residual = residual;
   p.ldr = ldr;
   p.pdl_late = t.lt;
+  p.red_alias = t.al;
   if (h->debug_count > 0) {
     --h->debug_count;
     p.debug_wait = 1;
@@ -513,6 +527,20 @@ std::vector<Tactic> candidates(const skinny_gemm_plan* h, int64_t M) {
             continue;
           }
           out.push_back(t);
+          // tcgen05 clusters: the variant whose receive buffer aliases the stages,
+          // when that lets more CTAs share an SM (it waits for the whole cluster's
+          // MMAs before reducing, so it only pays off through residency).
+          if (variant == kVariantTc && t.cl > 1) {
+            Tactic ta = t;
+            ta.al = 1;
+            const int per = h->dev->smem_per_sm;
+            const int rsv = h->dev->smem_reserved;
+            if (tactic_fits(h, ta, M, nullptr) &&
+                per / static_cast<int>(tactic_smem(ta) + rsv) >
+                    per / static_cast<int>(tactic_smem(t) + rsv) &&
+                active_clusters(h, ta) > 0)
+              out.push_back(ta);
+          }
         }
     }
   }

@@ -32,6 +32,8 @@ struct KParams {
   int32_t debug_wait;     // nonzero: watchdog self-test, wait on a dead barrier and return
   int32_t pdl_late;       // 0: launch dependents right after the first stages' weight loads;
                           // k >= 1: only once all but the last k-1 stages' loads are issued
+  int32_t red_alias;      // tcgen05 clusters: the reduction buffer reuses the pipeline stages
+  int32_t pad_;
   // stream-K kernel only: fp32 partial sums of split tiles and per-tile arrival counters
   float* workspace;       // [gridDim.x][2][TOK][128]
   uint32_t* counters;     // [ceil(N / 128)], zero between launches
@@ -77,9 +79,12 @@ const KernelEntry* sk_kernel_table(int* count);
 __host__ __device__ constexpr uint32_t tc_red_bytes(int tok) {
   return static_cast<uint32_t>(128 * (tok + 4) * 4);
 }
-// (The receive buffer exists only for clusters of more than one CTA.)
-__host__ __device__ constexpr uint32_t tc_smem_bytes(int tok, int nbox, int stages, int cluster) {
-  return kSmemAlign + stages * stage_bytes(128, tok, nbox) + (cluster > 1 ? tc_red_bytes(tok) : 0u) +
+// (The receive buffer exists only for clusters of more than one CTA, and takes
+// no space of its own when it aliases the pipeline stages.)
+__host__ __device__ constexpr uint32_t tc_smem_bytes(int tok, int nbox, int stages, int cluster,
+                                                     bool alias = false) {
+  return kSmemAlign + stages * stage_bytes(128, tok, nbox) +
+         (cluster > 1 && !alias ? tc_red_bytes(tok) : 0u) +
          static_cast<uint32_t>((2 * stages + 4) * 8) + 16;
 }
 

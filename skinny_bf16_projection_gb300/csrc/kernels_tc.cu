@@ -49,8 +49,12 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
   uint8_t* const gbase = smem_raw + (base - raw);
   const int S = p.stages;
   const uint32_t csize = cluster_nctarank();
-  const uint32_t red = base + static_cast<uint32_t>(S) * kStage;
-  const uint32_t bars = red + (csize > 1 ? tc_red_bytes(TOK) : 0u);
+  // With red_alias the cluster receive buffer lives in the pipeline stages,
+  // which are idle once every MMA has completed; peers push into it only after
+  // the cluster barrier that each CTA arrives at from that point on.
+  const bool alias = p.red_alias != 0 && csize > 1;
+  const uint32_t stages_end = base + static_cast<uint32_t>(S) * kStage;
+  const uint32_t bars = stages_end + (csize > 1 && !alias ? tc_red_bytes(TOK) : 0u);
   const uint32_t done_bar = bars + 8u * (2 * S);
   const uint32_t recv_bar = done_bar + 8u;
   const uint32_t dbg_bar = done_bar + 16u;
@@ -89,7 +93,11 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
   // [TOK][RS] fp32 blocks staged in the idle pipeline buffers (when they are
   // large enough); for smaller tiles per-thread st.async pushes, which measured
   // faster there.
-  const bool bulk = csize > 1 && TOK >= 64 && static_cast<uint32_t>(S) * kStage >= kStageRed;
+  const bool bulk = csize > 1 && TOK >= 64 &&
+                    static_cast<uint32_t>(S) * kStage >= (alias ? 2u : 1u) * kStageRed;
+  // Receive buffer: after the stages, or (aliased) at their start, or right
+  // after the bulk path's staging area.
+  const uint32_t red = !alias ? stages_end : (bulk ? base + kStageRed : base);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -111,7 +119,8 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot_g;
-  if (csize > 1) cluster_arrive_release();  // matched by the wait before the pushes
+  // matched by the wait before the pushes (aliased: arrive once the MMAs are done)
+  if (csize > 1 && !alias) cluster_arrive_release();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -194,6 +203,7 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
   pdl_wait();
   if (!mbar_wait_bounded(done_bar, 0, p.timeout_ns)) report_status(p.status, kStatusTimeoutDone);
   tc_fence_after_sync();
+  if (alias) cluster_arrive_release();  // this CTA's stages may now receive peers' partials
   // The accumulator is read 32 TMEM columns (tokens) at a time, so registers
   // stay bounded for token tiles up to 256.
   constexpr int CH = TOK < 32 ? TOK : 32;

@@ -376,7 +376,7 @@ def test_late_pdl_trigger_chain_matches_no_pdl():
             torch.cuda.synchronize()
             for k in (1, 2, 3, 4):
                 with_pdl.set_tactic(M, f"{base}:d{k}")
-                assert with_pdl.plan(M) == f"{base}:d{k}"
+                assert f"d{k}" in with_pdl.plan(M).split(":")
                 bufs = [ref[0]] + [torch.full((M, D), float("nan"), dtype=torch.bfloat16,
                                               device=DEV) for _ in range(links)]
                 for i in range(links):
