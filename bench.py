@@ -362,11 +362,13 @@ def other_workloads(torch, skg, pin, dev, l2, peak_gbs):
             sM = (1, 4, 8, 16, 32)
             for tuned in (False, True):  # default F_A plans first, for both chain lengths
                 for chain in (1, 4):
-                    if tuned:  # F_A tactic chosen by timing the whole step
+                    if tuned:  # F_A and main tactics chosen by timing the whole step
                         skg.tune_overlap(p16[0], fa[0], fb, list(sM), chain=chain)
                         for M in sM:
                             for p in fa[1:]:
                                 p.set_tactic(M, fa[0].plan(M))
+                            for p in p16[1:]:
+                                p.set_tactic(M, p16[0].plan(M))
                     for M in sM:
                         xm = xd[:M].contiguous()
                         om = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
@@ -381,11 +383,11 @@ def other_workloads(torch, skg, pin, dev, l2, peak_gbs):
                                                       chain=chain, aux_stream=aux, events=ev),
                             R * max(1, math.ceil(24 / R)))
                         alg = wbytes + 1536 * 128 * 2 * chain
-                        key = f"chain{chain}_M{M}" + ("_fa_tuned_in_step" if tuned else "")
+                        key = f"chain{chain}_M{M}" + ("_tuned_in_step" if tuned else "")
                         step[key] = {"step_us": round(us, 3),
                                      "weight_GBps": round(alg / us / 1e3, 1),
                                      "frac": round(alg / us / 1e3 / peak_gbs, 4),
-                                     "fa_tactic": fa[0].plan(M)}
+                                     "fa_tactic": fa[0].plan(M), "main_tactic": p16[0].plan(M)}
             res["overlap step: W[6288,7168] main || F_A[128,7168] -> F_B[1536,128] aux"] = step
             for p in fa:
                 p.close()

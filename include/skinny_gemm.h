@@ -173,15 +173,16 @@ int skinny_gemm_run_overlap(skinny_gemm_t h_main, skinny_gemm_t h_fa, skinny_gem
 int skinny_gemm_autotune(skinny_gemm_t h, const int64_t* Ms, int nM, void* stream);
 
 /*
- * Tune the F_A projection of the two-stream step for concurrency: for each M in
- * Ms, every candidate F_A tactic is timed inside the whole step (main
- * projection rotating over scratch copies of its weight, F_A -> F_B chain on a
- * high-priority aux stream, fork/join by events), as a CUDA graph of
- * back-to-back steps, and the one with the shortest step is installed in
- * h_fa's plan.  (A tactic that is fastest alone can be slow next to a grid
- * that fills the GPU.)  Main and F_B keep their plans.  Same rules as
- * skinny_gemm_autotune: synchronizes `stream`, allocates and frees scratch,
- * not while capturing.
+ * Tune the two-stream step for concurrency: for each M in Ms, the candidate
+ * tactics of F_A, then of the main projection, then of F_A again are each
+ * timed inside the whole step (main projection rotating over scratch copies of
+ * its weight, F_A -> F_B chain on a high-priority aux stream, fork/join by
+ * events), as a CUDA graph of back-to-back steps, and the tactic with the
+ * shortest step is installed in h_fa's / h_main's plan.  (A tactic that is
+ * fastest alone can be slow next to a grid that fills the GPU; the main
+ * projection's step-tuned plan may be slower when it runs alone.)  F_B keeps
+ * its plan.  Same rules as skinny_gemm_autotune: synchronizes `stream`,
+ * allocates and frees scratch, not while capturing.
  */
 int skinny_gemm_autotune_overlap(skinny_gemm_t h_main, skinny_gemm_t h_fa, skinny_gemm_t h_fb,
                                  int chain, const int64_t* Ms, int nM, void* stream);

@@ -113,7 +113,8 @@ class Projection:
 
     # ---------------------------------------------------------------- plan
     def autotune(self, Ms: Iterable[int], stream=None) -> None:
-        arr = (ctypes.c_int64 * len(list(Ms)))(*list(Ms))
+        ms = list(Ms)
+        arr = (ctypes.c_int64 * len(ms))(*ms)
         with torch.cuda.device(self.device):
             _native.check(self._lib.skinny_gemm_autotune(self._h, arr, len(arr), _stream_ptr(stream)))
 
@@ -178,8 +179,8 @@ def run_overlap(main: Projection, fa: Projection, fb: Projection, x: torch.Tenso
 
 def tune_overlap(main: Projection, fa: Projection, fb: Projection, Ms: Iterable[int], *,
                  chain: int = 1, stream=None) -> None:
-    """Pick fa's tactic for each M by timing the whole two-stream step (see
-    skinny_gemm_autotune_overlap); main and fb keep their plans."""
+    """Pick fa's and main's tactics for each M by timing the whole two-stream
+    step (see skinny_gemm_autotune_overlap); fb keeps its plan."""
     ms = list(Ms)
     arr = (ctypes.c_int64 * len(ms))(*ms)
     with torch.cuda.device(main.device):

@@ -960,67 +960,99 @@ int skinny_gemm_autotune_overlap(skinny_gemm_t h_main, skinny_gemm_t h_fa, skinn
       return code;
     }
   }
+  // One step = the whole two-stream step, timed as a graph of L back-to-back
+  // steps (the main projection rotating over the scratch copies).
+  auto time_step = [&](int64_t M, double* us_out) -> int {
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    cudaError_t ce = cudaStreamBeginCapture(ts, cudaStreamCaptureModeThreadLocal);
+    if (ce != cudaSuccess) return cuda_fail(ce, "cudaStreamBeginCapture(autotune_overlap)");
+    int trc = SKG_OK;
+    for (int l = 0; l < L && trc == SKG_OK; ++l)
+      trc = skinny_gemm_run_overlap(&shadow[l % R], h_fa, h_fb, chain, xb, M, om, fo, fbo, ts, as,
+                                    fork, join);
+    ce = cudaStreamEndCapture(ts, &graph);
+    if (trc != SKG_OK || ce != cudaSuccess) {
+      if (graph) cudaGraphDestroy(graph);
+      return trc != SKG_OK ? trc : cuda_fail(ce, "cudaStreamEndCapture(autotune_overlap)");
+    }
+    ce = cudaGraphInstantiate(&exec, graph, 0);
+    if (ce != cudaSuccess) {
+      cudaGraphDestroy(graph);
+      return cuda_fail(ce, "cudaGraphInstantiate(autotune_overlap)");
+    }
+    float best_ms = 1e30f;
+    ce = cudaGraphLaunch(exec, ts);
+    for (int r = 0; r < 3 && ce == cudaSuccess; ++r) {
+      cudaEventRecord(e0, ts);
+      ce = cudaGraphLaunch(exec, ts);
+      cudaEventRecord(e1, ts);
+      if (ce == cudaSuccess) ce = cudaEventSynchronize(e1);
+      float ms = 0;
+      if (ce == cudaSuccess && cudaEventElapsedTime(&ms, e0, e1) == cudaSuccess)
+        best_ms = std::min(best_ms, ms);
+    }
+    cudaGraphExecDestroy(exec);
+    cudaGraphDestroy(graph);
+    if (ce != cudaSuccess) return cuda_fail(ce, "autotune_overlap timing");
+    *us_out = 1000.0 * best_ms / L;
+    return SKG_OK;
+  };
+  // The main projection's tactic for M, on the handle and on every shadow.
+  auto set_main = [&](int64_t M, const Tactic& t) -> int {
+    const int wrc = ensure_workspace(h_main, t);
+    if (wrc != SKG_OK) return wrc;
+    h_main->plan[M] = t;
+    for (skinny_gemm_plan& sh : shadow) {
+      sh.plan[M] = t;
+      sh.workspace = h_main->workspace;
+      sh.workspace_bytes = h_main->workspace_bytes;
+      sh.counters = h_main->counters;
+      sh.counters_bytes = h_main->counters_bytes;
+    }
+    return SKG_OK;
+  };
   int rc = SKG_OK;
   std::vector<int64_t> tuned;
   for (int i = 0; i < nM && rc == SKG_OK; ++i) {
     const int64_t M = Ms[i];
-    const Tactic keep = h_fa->plan[M];
-    double best_us = 1e30;
-    Tactic best;
-    for (const Tactic& t : candidates(h_fa, M)) {
-      rc = ensure_workspace(h_fa, t);
-      if (rc != SKG_OK) break;
-      h_fa->plan[M] = t;
-      cudaGraph_t graph = nullptr;
-      cudaGraphExec_t exec = nullptr;
-      e = cudaStreamBeginCapture(ts, cudaStreamCaptureModeThreadLocal);
-      if (e != cudaSuccess) {
-        rc = cuda_fail(e, "cudaStreamBeginCapture(autotune_overlap)");
-        break;
+    double step_us = 0;
+    // Passes: F_A's tactic (main fixed), the main projection's (F_A fixed), F_A's again.
+    for (int pass = 0; pass < 3 && rc == SKG_OK; ++pass) {
+      const bool fa_pass = pass != 1;
+      skinny_gemm_t hp = fa_pass ? h_fa : h_main;
+      const Tactic keep = hp->plan[M];
+      double best_us = 1e30;
+      Tactic best;
+      for (const Tactic& t : candidates(hp, M)) {
+        rc = fa_pass ? ensure_workspace(h_fa, t) : set_main(M, t);
+        if (rc != SKG_OK) break;
+        if (fa_pass) h_fa->plan[M] = t;
+        double us = 0;
+        rc = time_step(M, &us);
+        if (rc != SKG_OK) break;
+        if (log_enabled())
+          fprintf(stderr, "[skinny_gemm] tune overlap M=%lld %s %s: step %.3f us\n",
+                  static_cast<long long>(M), fa_pass ? "F_A" : "main", tactic_str(t).c_str(), us);
+        if (us < best_us) {
+          best_us = us;
+          best = t;
+        }
       }
-      for (int l = 0; l < L && rc == SKG_OK; ++l)
-        rc = skinny_gemm_run_overlap(&shadow[l % R], h_fa, h_fb, chain, xb, M, om, fo, fbo, ts, as,
-                                     fork, join);
-      e = cudaStreamEndCapture(ts, &graph);
-      if (rc != SKG_OK || e != cudaSuccess) {
-        if (graph) cudaGraphDestroy(graph);
-        if (rc == SKG_OK) rc = cuda_fail(e, "cudaStreamEndCapture(autotune_overlap)");
-        break;
+      const Tactic pick = (rc == SKG_OK && best.valid()) ? best : keep;
+      if (fa_pass) {
+        h_fa->plan[M] = pick;
+      } else {
+        const int src = set_main(M, pick);
+        if (rc == SKG_OK) rc = src;
       }
-      e = cudaGraphInstantiate(&exec, graph, 0);
-      if (e != cudaSuccess) {
-        cudaGraphDestroy(graph);
-        rc = cuda_fail(e, "cudaGraphInstantiate(autotune_overlap)");
-        break;
-      }
-      float best_ms = 1e30f;
-      e = cudaGraphLaunch(exec, ts);
-      for (int r = 0; r < 3 && e == cudaSuccess; ++r) {
-        cudaEventRecord(e0, ts);
-        e = cudaGraphLaunch(exec, ts);
-        cudaEventRecord(e1, ts);
-        if (e == cudaSuccess) e = cudaEventSynchronize(e1);
-        float ms = 0;
-        if (e == cudaSuccess && cudaEventElapsedTime(&ms, e0, e1) == cudaSuccess)
-          best_ms = std::min(best_ms, ms);
-      }
-      cudaGraphExecDestroy(exec);
-      cudaGraphDestroy(graph);
-      if (e != cudaSuccess) {
-        rc = cuda_fail(e, "autotune_overlap timing");
-        break;
-      }
-      const double us = 1000.0 * best_ms / L;
-      if (log_enabled())
-        fprintf(stderr, "[skinny_gemm] tune overlap M=%lld F_A %s: step %.3f us\n",
-                static_cast<long long>(M), tactic_str(t).c_str(), us);
-      if (us < best_us) {
-        best_us = us;
-        best = t;
-      }
+      step_us = best_us;
     }
-    h_fa->plan[M] = (rc == SKG_OK && best.valid()) ? best : keep;
-    if (rc == SKG_OK && best.valid()) tuned.push_back(M);
+    if (rc == SKG_OK) tuned.push_back(M);
+    if (log_enabled() && rc == SKG_OK)
+      fprintf(stderr, "[skinny_gemm] overlap M=%lld: main %s, F_A %s, step %.3f us\n",
+              static_cast<long long>(M), tactic_str(h_main->plan[M]).c_str(),
+              tactic_str(h_fa->plan[M]).c_str(), step_us);
   }
   cleanup();
   if (rc != SKG_OK) return rc;
@@ -1030,6 +1062,7 @@ int skinny_gemm_autotune_overlap(skinny_gemm_t h_main, skinny_gemm_t h_fa, skinn
     for (int64_t mp : tuned)
       if (mp >= m) {
         if (tactic_fits(h_fa, h_fa->plan[mp], m, nullptr)) h_fa->plan[m] = h_fa->plan[mp];
+        if (tactic_fits(h_main, h_main->plan[mp], m, nullptr)) h_main->plan[m] = h_main->plan[mp];
         break;
       }
   }
