@@ -18,6 +18,7 @@ import hashlib
 import json
 import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -186,6 +187,42 @@ def oracle_step_rate(seconds: float, sweep=SWEEP, N=N_DEC, K=K_DEC):
     return gbs, cores, sample, per_sweep
 
 
+def oracle_single_thread(seconds: float = 3.0, sweep=SWEEP, N=N_DEC, K=K_DEC):
+    """The same oracle on one host thread, over a 64-row sample of W (weight GB/s)."""
+    import oracle
+    import projection_inputs as pin
+    w, x = pin.case(N, K, seed=0)
+    ws = w[:64]
+    sweeps = 0
+    t0 = time.perf_counter()
+    while True:
+        for M in sweep:
+            oracle.projection(x[:M], ws, with_scale=False, threads=1)
+        sweeps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return sweeps * len(sweep) * ws.shape[0] * K * 2 / el / 1e9
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine()
+
+
 # ----------------------------------------------------------------------------- reference arm
 def reference_arm(args, rank, world):
     """The oracle timed as it stands on the host cores.  One step = one sweep of
@@ -306,6 +343,13 @@ def other_workloads(torch, skg, pin, dev, l2, peak_gbs):
                 entry[f"M{M}_{'bf16' if odt == torch.bfloat16 else 'fp32'}"] = {
                     "us": round(us, 3), "weight_GBps": round(gbs, 1),
                     "frac": round(gbs / peak_gbs, 4), "tactic": projs[0].plan(M)}
+        # secondary, labelled: the same weight back to back (L2-assisted: it stays in L2)
+        for M in (1, 8, 32):
+            out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            xm = xd[:M].contiguous()
+            us = graph_time_us(torch, stream, dev, lambda i: p16[0].run(xm, out), 48)
+            entry[f"M{M}_bf16_same_weight_L2_assisted"] = {"us": round(us, 3),
+                                                           "weight_GBps": round(wbytes / us / 1e3, 1)}
         # context only (not part of this library): cuBLAS through torch.mm, same rotation
         for M in (1, 8, 32, 64, 128, 256):
             out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
@@ -630,7 +674,9 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         gbs, cores, sample, _ = oracle_step_rate(args.cpu_seconds)
         line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores,
-                                "kind": "oracle", "sample": sample}
+                                "kind": "oracle", "sample": sample,
+                                "single_thread_value": round(oracle_single_thread(), 4),
+                                "cpu_model": cpu_model()}
     if rank == 0:
         print(json.dumps(line), flush=True)
     barrier(world)
