@@ -137,6 +137,16 @@ int skinny_gemm_run_residual(skinny_gemm_t h, const void* x, int64_t ldx, int64_
 int skinny_gemm_run_host(skinny_gemm_t h, const void* x_host, int64_t M, void* out_host,
                          void* stream);
 
+/* The same three steps as skinny_gemm_run_host (H2D of x into the handle's
+ * staging buffer, the projection, D2H of out), enqueued on `stream` without
+ * waiting: the caller synchronizes the stream before reading out_host, and
+ * keeps both host buffers alive until then.  Pinned host memory makes the
+ * copies asynchronous (pageable memory works but the copies then block).  Two
+ * calls on one handle must be on the same stream (they share the staging
+ * buffers).  The first call per handle allocates the staging buffers. */
+int skinny_gemm_run_host_async(skinny_gemm_t h, const void* x_host, int64_t M, void* out_host,
+                               void* stream);
+
 /*
  * The two-stream decode step (low_latency_gemm page, run_kda_projection_overlap:
  * hidden [M, 7168], packed Q/K/V/G/F_A/beta weight [6288, 7168], F_B weight

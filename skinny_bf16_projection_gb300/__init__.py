@@ -99,17 +99,33 @@ class Projection:
             out = torch.empty((x.shape[0], self.N), dtype=self.out_dtype, device=x.device)
         return self.run(x, out, stream)
 
-    def run_host(self, x_host: torch.Tensor, out_host: torch.Tensor, stream=None) -> torch.Tensor:
-        """End-to-end call with host (ideally pinned) buffers; synchronizes the stream."""
+    def _check_host(self, x_host: torch.Tensor, out_host: torch.Tensor) -> None:
         if x_host.is_cuda or out_host.is_cuda:
             raise ValueError("run_host takes host tensors")
         if not (x_host.is_contiguous() and out_host.is_contiguous()):
             raise ValueError("run_host needs packed host buffers")
+        if x_host.dim() != 2 or x_host.shape[1] != self.K or x_host.dtype != self.weight.dtype:
+            raise ValueError(f"x_host must be [M, {self.K}] {self.weight.dtype}")
+        if tuple(out_host.shape) != (x_host.shape[0], self.N) or out_host.dtype != self.out_dtype:
+            raise ValueError(f"out_host must be [M, {self.N}] {self.out_dtype}")
+
+    def run_host(self, x_host: torch.Tensor, out_host: torch.Tensor, stream=None) -> torch.Tensor:
+        """End-to-end call with host (ideally pinned) buffers; synchronizes the stream."""
+        self._check_host(x_host, out_host)
         with torch.cuda.device(self.device):
             _native.check(self._lib.skinny_gemm_run_host(
                 self._h, x_host.data_ptr(), x_host.shape[0], out_host.data_ptr(),
                 _stream_ptr(stream)))
         return out_host
+
+    def run_host_async(self, x_host: torch.Tensor, out_host: torch.Tensor, stream=None) -> None:
+        """Enqueue copy-in, projection and copy-out on the stream without waiting
+        (pinned host buffers; synchronize the stream before reading out_host)."""
+        self._check_host(x_host, out_host)
+        with torch.cuda.device(self.device):
+            _native.check(self._lib.skinny_gemm_run_host_async(
+                self._h, x_host.data_ptr(), x_host.shape[0], out_host.data_ptr(),
+                _stream_ptr(stream)))
 
     # ---------------------------------------------------------------- plan
     def autotune(self, Ms: Iterable[int], stream=None) -> None:

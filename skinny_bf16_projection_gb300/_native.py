@@ -29,6 +29,7 @@ SIGNATURES = [
     ("skinny_gemm_run_strided", _int, [_vp, _vp, _i64, _i64, _vp, _i64, _vp]),
     ("skinny_gemm_run_residual", _int, [_vp, _vp, _i64, _i64, _vp, _i64, _vp, _i64, _vp]),
     ("skinny_gemm_run_host", _int, [_vp, _vp, _i64, _vp, _vp]),
+    ("skinny_gemm_run_host_async", _int, [_vp, _vp, _i64, _vp, _vp]),
     ("skinny_gemm_run_overlap", _int, [_vp, _vp, _vp, _int, _vp, _i64, _vp, _vp, _vp, _vp, _vp,
                                        _vp, _vp]),
     ("skinny_gemm_autotune", _int, [_vp, ctypes.POINTER(_i64), _int, _vp]),

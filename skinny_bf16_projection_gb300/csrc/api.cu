@@ -809,14 +809,15 @@ int skinny_gemm_run(skinny_gemm_t h, const void* x, int64_t M, void* out, void* 
   return skinny_gemm_run_strided(h, x, h->K, M, out, h->N, stream);
 }
 
-int skinny_gemm_run_host(skinny_gemm_t h, const void* x_host, int64_t M, void* out_host,
-                         void* stream) {
+namespace {
+// H2D of x into the handle's staging buffer, the projection, D2H of out, all
+// enqueued on `st` (staging allocated on first use).
+int enqueue_host(skinny_gemm_t h, const void* x_host, int64_t M, void* out_host, cudaStream_t st) {
   if (check_handle(h) != SKG_OK) return SKG_EINVAL;
   if (x_host == nullptr || out_host == nullptr) return fail(SKG_EINVAL, "null host buffer");
   if (M < 1 || M > SKINNY_GEMM_MAX_M)
     return fail(SKG_EUNSUPPORTED_M, "M = %lld outside 1..%d", static_cast<long long>(M),
                 SKINNY_GEMM_MAX_M);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (h->x_stage == nullptr) {
     e = cudaMalloc(&h->x_stage, static_cast<size_t>(SKINNY_GEMM_MAX_M) * h->K * 2);
@@ -828,14 +829,29 @@ int skinny_gemm_run_host(skinny_gemm_t h, const void* x_host, int64_t M, void* o
   }
   e = cudaMemcpyAsync(h->x_stage, x_host, static_cast<size_t>(M) * h->K * 2, cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(x)");
-  int rc = skinny_gemm_run(h, h->x_stage, M, h->out_stage, stream);
+  int rc = skinny_gemm_run(h, h->x_stage, M, h->out_stage, st);
   if (rc != SKG_OK) return rc;
   e = cudaMemcpyAsync(out_host, h->out_stage, static_cast<size_t>(M) * h->N * out_elem_bytes(h),
                       cudaMemcpyDeviceToHost, st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(out)");
-  e = cudaStreamSynchronize(st);
+  return SKG_OK;
+}
+}  // namespace
+
+int skinny_gemm_run_host(skinny_gemm_t h, const void* x_host, int64_t M, void* out_host,
+                         void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int rc = enqueue_host(h, x_host, M, out_host, st);
+  if (rc != SKG_OK) return rc;
+  const cudaError_t e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
   return ok();
+}
+
+int skinny_gemm_run_host_async(skinny_gemm_t h, const void* x_host, int64_t M, void* out_host,
+                               void* stream) {
+  const int rc = enqueue_host(h, x_host, M, out_host, static_cast<cudaStream_t>(stream));
+  return rc != SKG_OK ? rc : ok();
 }
 
 int skinny_gemm_run_overlap(skinny_gemm_t h_main, skinny_gemm_t h_fa, skinny_gemm_t h_fb, int chain,

@@ -231,6 +231,27 @@ def test_run_host_end_to_end():
         assert_parity(oh, ref[:M], s[:M], f"run_host M={M}")
 
 
+def test_run_host_async_pipelined_calls():
+    """Several asynchronous host-buffer calls on one stream (pinned buffers, one
+    synchronize at the end), two on the same handle, each output checked."""
+    w, x, ref, s = full_case(3584, 7168)
+    wd = w.to(DEV)
+    projs = [skg().Projection(wd, use_tactic_file=False) for _ in range(2)]
+    st = torch.cuda.Stream()
+    Ms = (1, 8, 16, 32, 5)
+    xh = {M: x[:M].contiguous().pin_memory() for M in Ms}
+    oh = {M: torch.full((M, 3584), float("nan"), dtype=torch.bfloat16).pin_memory() for M in Ms}
+    for i, M in enumerate(Ms):
+        projs[i % 2].run_host_async(xh[M], oh[M], st)
+    st.synchronize()
+    for M in Ms:
+        assert_parity(oh[M], ref[:M], s[:M], f"run_host_async M={M}")
+    with pytest.raises(ValueError):  # K mismatch is refused before any copy
+        projs[0].run_host_async(x[:4, :100].contiguous(), oh[5][:4].contiguous(), st)
+    for p in projs:
+        p.close()
+
+
 def test_autotune_installs_a_valid_plan():
     w, x, ref, s = full_case(3584, 7168)
     proj = skg().Projection(w.to(DEV), use_tactic_file=False)
