@@ -429,31 +429,37 @@ int launch_tactic(skinny_gemm_plan* h, const Tactic& t, const void* x, int64_t l
   return SKG_OK;
 }
 
+// CTAs of this tactic one SM holds at once, counted from shared memory,
+// registers, threads and tensor-memory columns (0: cannot launch).  Counted
+// here rather than by cudaOccupancyMaxActiveBlocksPerMultiprocessor, which
+// answers one block per SM for any kernel that allocates tensor memory
+// (measured: four such blocks of 32 columns ran at once per SM).
+int resident_per_sm(const skinny_gemm_plan* h, const Tactic& t) {
+  const KernelEntry* k = find_kernel(t, h->dtype, h->out_dtype);
+  if (k == nullptr) return 0;
+  cudaFuncAttributes fa{};
+  if (cudaFuncGetAttributes(&fa, k->func) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  const DeviceInfo& d = *h->dev;
+  const int regs = ((fa.numRegs + 7) / 8) * 8 * k->threads;
+  int per_sm = std::min(32, d.threads_per_sm / k->threads);
+  per_sm = std::min(per_sm, regs > 0 ? d.regs_per_sm / regs : per_sm);
+  per_sm = std::min(per_sm, d.smem_per_sm / static_cast<int>(tactic_smem(t) + d.smem_reserved));
+  const int tmem_cols = t.variant == kVariantSk  ? (2 * t.tok <= 32 ? 32 : (2 * t.tok <= 64 ? 64 : 128))
+                        : t.variant == kVariantTc ? std::max(32, t.tok)
+                                                  : 0;
+  if (tmem_cols > 0) per_sm = std::min(per_sm, 512 / tmem_cols);
+  return std::max(per_sm, 0);
+}
+
 // Clusters of this tactic that fit on the GPU at once (0: cannot launch).
 // Without clusters this is resident CTAs per SM x SMs.
 int active_clusters(const skinny_gemm_plan* h, const Tactic& t) {
   const KernelEntry* k = find_kernel(t, h->dtype, h->out_dtype);
   if (k == nullptr) return 0;
-  if (tactic_cluster(t) == 1) {
-    // Counted here rather than by cudaOccupancyMaxActiveBlocksPerMultiprocessor,
-    // which answers one block per SM for any kernel that allocates tensor
-    // memory (measured: four such blocks of 32 columns ran at once per SM).
-    cudaFuncAttributes fa{};
-    if (cudaFuncGetAttributes(&fa, k->func) != cudaSuccess) {
-      (void)cudaGetLastError();
-      return 0;
-    }
-    const DeviceInfo& d = *h->dev;
-    const int regs = ((fa.numRegs + 7) / 8) * 8 * k->threads;
-    int per_sm = std::min(32, d.threads_per_sm / k->threads);
-    per_sm = std::min(per_sm, regs > 0 ? d.regs_per_sm / regs : per_sm);
-    per_sm = std::min(per_sm, d.smem_per_sm / static_cast<int>(tactic_smem(t) + d.smem_reserved));
-    const int tmem_cols = t.variant == kVariantSk  ? (2 * t.tok <= 32 ? 32 : (2 * t.tok <= 64 ? 64 : 128))
-                          : t.variant == kVariantTc ? std::max(32, t.tok)
-                                                    : 0;
-    if (tmem_cols > 0) per_sm = std::min(per_sm, 512 / tmem_cols);
-    return std::max(per_sm, 0) * d.sm_count;
-  }
+  if (tactic_cluster(t) == 1) return resident_per_sm(h, t) * h->dev->sm_count;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(tactic_grid(h, t)), 1, 1);
   cfg.blockDim = dim3(static_cast<unsigned>(k->threads), 1, 1);
@@ -555,7 +561,9 @@ std::vector<Tactic> candidates(const skinny_gemm_plan* h, int64_t M) {
 //   M <= 64  tcgen05, 64-token tile, 1 box x 3 stages
 // with the cluster split (split-K factor) that gives about 1.4 CTAs per SM
 // (64-row tiles: at most 3), at most 8; fewer stages where shared memory or
-// the K range is short.  Any
+// the K range is short, or where the grid would not be resident in one wave
+// (then 3 -> 2 stages, then half the cluster: e.g. the 6288x7168 weight runs
+// 2 stages for its 8-token tile and clusters of 4 for its 32/64-token tiles).  Any
 // choice that does not fit falls back to fewer stages, then to the tcgen05
 // kernel with the same rule.
 Tactic default_tactic(const skinny_gemm_plan* h, int64_t M) {
@@ -575,9 +583,21 @@ Tactic default_tactic(const skinny_gemm_plan* h, int64_t M) {
     // Late PDL trigger (measured on the 3584x7168 and 6288x7168 weights): with
     // 2 (tcgen05) or 3 (mma.sync) stages still to issue.
     t.lt = t.variant == kVariantMma ? 3 : 2;
-    for (; t.stages >= 1; --t.stages)
-      if (tactic_fits(h, t, M, nullptr)) return t;
-    return Tactic{};
+    // Fewer stages (down to 2), then a smaller cluster, until the whole grid is
+    // resident at once (one wave); else the first tactic that fits.
+    Tactic fit;
+    const int s0 = t.stages;
+    for (; t.cl >= 1; t.cl /= 2) {
+      for (t.stages = s0; t.stages >= 1; --t.stages) {
+        if (!tactic_fits(h, t, M, nullptr)) continue;
+        if (!fit.valid()) fit = t;
+        // (per-SM count: the cluster occupancy query undercounts tensor-memory kernels)
+        const int64_t resident = static_cast<int64_t>(resident_per_sm(h, t)) * h->dev->sm_count;
+        if (resident >= tactic_grid(h, t)) return t;
+        if (t.stages <= 2) break;
+      }
+    }
+    return fit;
   };
   Tactic t;
   if (M <= 8)
