@@ -231,7 +231,11 @@ int skinny_gemm_check_status(skinny_gemm_t h, void* stream);
 int skinny_gemm_debug_inject_timeout(skinny_gemm_t h, int count, uint64_t timeout_ns);
 
 /* Release the handle (its status word and staging buffers).  The caller must
- * make sure no launch using it is still pending.  NULL is ignored. */
+ * make sure no launch using it is still pending.  NULL, an already destroyed
+ * handle and a pointer that never was a handle are ignored.  Every entry point
+ * refuses a destroyed or unknown handle with SKG_EINVAL (the library keeps a
+ * set of live handles; an address reused by a later prepare counts as that
+ * new handle). */
 void skinny_gemm_destroy(skinny_gemm_t h);
 
 /*

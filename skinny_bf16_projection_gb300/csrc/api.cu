@@ -13,6 +13,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <unordered_set>
 #include <vector>
 
 #include "kernel_params.h"
@@ -662,14 +663,36 @@ void append_tactic_file(const skinny_gemm_plan* h, int64_t M, const Tactic& t, d
   fclose(f);
 }
 
+// Live handles (prepare inserts, destroy erases), so that a destroyed or
+// foreign pointer is refused with EINVAL instead of being dereferenced.  An
+// address reused by a later prepare is indistinguishable from that handle.
+std::mutex g_handles_mu;
+std::unordered_set<const skinny_gemm_plan*>& live_handles() {
+  static std::unordered_set<const skinny_gemm_plan*> s;
+  return s;
+}
+void register_handle(const skinny_gemm_plan* h) {
+  std::lock_guard<std::mutex> lk(g_handles_mu);
+  live_handles().insert(h);
+}
+bool unregister_handle(const skinny_gemm_plan* h) {
+  std::lock_guard<std::mutex> lk(g_handles_mu);
+  return live_handles().erase(h) > 0;
+}
+
 int check_handle(const skinny_gemm_plan* h) {
   if (h == nullptr) return fail(SKG_EINVAL, "null handle");
+  {
+    std::lock_guard<std::mutex> lk(g_handles_mu);
+    if (live_handles().count(h) == 0) return fail(SKG_EINVAL, "unknown or destroyed handle");
+  }
   return SKG_OK;
 }
 
-int validate_run(const skinny_gemm_plan* h, const void* x, int64_t ldx, int64_t M, const void* out,
-                 int64_t ldo) {
-  if (check_handle(h) != SKG_OK) return SKG_EINVAL;
+// Argument checks of a run on a plan (the handle itself is checked by callers
+// of the public entry points; the tuners pass private copies of a plan).
+int validate_args(const skinny_gemm_plan* h, const void* x, int64_t ldx, int64_t M, const void* out,
+                  int64_t ldo) {
   if (M < 1 || M > SKINNY_GEMM_MAX_M)
     return fail(SKG_EUNSUPPORTED_M, "M = %lld outside 1..%d: fall back", static_cast<long long>(M),
                 SKINNY_GEMM_MAX_M);
@@ -682,6 +705,12 @@ int validate_run(const skinny_gemm_plan* h, const void* x, int64_t ldx, int64_t 
     return fail(SKG_EALIGN, "x and out must be 16-byte aligned");
   if ((ldx * 2) % 16) return fail(SKG_EALIGN, "x row pitch must be a multiple of 16 bytes");
   return SKG_OK;
+}
+
+int validate_run(const skinny_gemm_plan* h, const void* x, int64_t ldx, int64_t M, const void* out,
+                 int64_t ldo) {
+  if (check_handle(h) != SKG_OK) return SKG_EINVAL;
+  return validate_args(h, x, ldx, M, out, ldo);
 }
 
 }  // namespace
@@ -786,6 +815,7 @@ skinny_gemm_t skinny_gemm_prepare_ex(const void* W, int64_t N, int64_t K, int64_
     for (int m : {1, 2, 4, 8, 16, 32, 48, 64}) fprintf(stderr, " M%d=%s", m, tactic_str(h->plan[m]).c_str());
     fprintf(stderr, "\n");
   }
+  register_handle(h);
   ok();
   return h;
 }
@@ -874,12 +904,12 @@ int skinny_gemm_run_host_async(skinny_gemm_t h, const void* x_host, int64_t M, v
   return rc != SKG_OK ? rc : ok();
 }
 
-int skinny_gemm_run_overlap(skinny_gemm_t h_main, skinny_gemm_t h_fa, skinny_gemm_t h_fb, int chain,
-                            const void* x, int64_t M, void* out_main, void* fa, void* out_fb,
-                            void* main_stream, void* aux_stream, void* fork_event,
-                            void* join_event) {
-  if (h_main == nullptr || h_fa == nullptr || h_fb == nullptr)
-    return fail(SKG_EINVAL, "null handle");
+namespace {
+// The two-stream step on plans already known to be valid (public entry point
+// below; the overlap tuner passes private copies of the main plan).
+int overlap_impl(skinny_gemm_t h_main, skinny_gemm_t h_fa, skinny_gemm_t h_fb, int chain,
+                 const void* x, int64_t M, void* out_main, void* fa, void* out_fb,
+                 void* main_stream, void* aux_stream, void* fork_event, void* join_event) {
   if (chain < 1) return fail(SKG_EINVAL, "chain must be >= 1");
   if (h_fa->K != h_main->K) return fail(SKG_EINVAL, "F_A and main weights need the same K");
   if (h_fa->out_dtype != SKG_BF16) return fail(SKG_EINVAL, "F_A output must be bf16 (it feeds F_B)");
@@ -888,9 +918,9 @@ int skinny_gemm_run_overlap(skinny_gemm_t h_main, skinny_gemm_t h_fa, skinny_gem
     return fail(SKG_EINVAL, "a chain needs bf16 F_B output with N_fb >= K_fb");
   if (fork_event == nullptr || join_event == nullptr || aux_stream == nullptr)
     return fail(SKG_EINVAL, "overlap needs an aux stream and two events");
-  int rc = validate_run(h_main, x, h_main->K, M, out_main, h_main->N);
+  int rc = validate_args(h_main, x, h_main->K, M, out_main, h_main->N);
   if (rc != SKG_OK) return rc;
-  rc = validate_run(h_fa, x, h_fa->K, M, fa, h_fa->N);
+  rc = validate_args(h_fa, x, h_fa->K, M, fa, h_fa->N);
   if (rc != SKG_OK) return rc;
   cudaStream_t ms = static_cast<cudaStream_t>(main_stream);
   cudaStream_t as = static_cast<cudaStream_t>(aux_stream);
@@ -919,10 +949,22 @@ int skinny_gemm_run_overlap(skinny_gemm_t h_main, skinny_gemm_t h_fa, skinny_gem
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent(main, join)");
   return ok();
 }
+}  // namespace
+
+int skinny_gemm_run_overlap(skinny_gemm_t h_main, skinny_gemm_t h_fa, skinny_gemm_t h_fb, int chain,
+                            const void* x, int64_t M, void* out_main, void* fa, void* out_fb,
+                            void* main_stream, void* aux_stream, void* fork_event,
+                            void* join_event) {
+  if (check_handle(h_main) != SKG_OK || check_handle(h_fa) != SKG_OK || check_handle(h_fb) != SKG_OK)
+    return SKG_EINVAL;
+  return overlap_impl(h_main, h_fa, h_fb, chain, x, M, out_main, fa, out_fb, main_stream,
+                      aux_stream, fork_event, join_event);
+}
 
 int skinny_gemm_autotune_overlap(skinny_gemm_t h_main, skinny_gemm_t h_fa, skinny_gemm_t h_fb,
                                  int chain, const int64_t* Ms, int nM, void* stream) {
-  if (h_main == nullptr || h_fa == nullptr || h_fb == nullptr) return fail(SKG_EINVAL, "null handle");
+  if (check_handle(h_main) != SKG_OK || check_handle(h_fa) != SKG_OK || check_handle(h_fb) != SKG_OK)
+    return SKG_EINVAL;
   if (chain < 1) return fail(SKG_EINVAL, "chain must be >= 1");
   if (h_fa->K != h_main->K || h_fb->K != h_fa->N || h_fa->out_dtype != SKG_BF16 ||
       h_main->dtype != h_fa->dtype)
@@ -1005,8 +1047,7 @@ int skinny_gemm_autotune_overlap(skinny_gemm_t h_main, skinny_gemm_t h_fa, skinn
     if (ce != cudaSuccess) return cuda_fail(ce, "cudaStreamBeginCapture(autotune_overlap)");
     int trc = SKG_OK;
     for (int l = 0; l < L && trc == SKG_OK; ++l)
-      trc = skinny_gemm_run_overlap(&shadow[l % R], h_fa, h_fb, chain, xb, M, om, fo, fbo, ts, as,
-                                    fork, join);
+      trc = overlap_impl(&shadow[l % R], h_fa, h_fb, chain, xb, M, om, fo, fbo, ts, as, fork, join);
     ce = cudaStreamEndCapture(ts, &graph);
     if (trc != SKG_OK || ce != cudaSuccess) {
       if (graph) cudaGraphDestroy(graph);
@@ -1342,7 +1383,7 @@ int skinny_gemm_debug_inject_timeout(skinny_gemm_t h, int count, uint64_t timeou
 }
 
 void skinny_gemm_destroy(skinny_gemm_t h) {
-  if (h == nullptr) return;
+  if (h == nullptr || !unregister_handle(h)) return;  // null, unknown or already destroyed
   if (h->status) cudaFree(h->status);
   if (h->workspace) cudaFree(h->workspace);
   if (h->counters) cudaFree(h->counters);

@@ -313,6 +313,31 @@ def test_error_codes():
     torch.cuda.synchronize()
 
 
+def test_destroyed_or_foreign_handle_is_refused():
+    """A destroyed handle (and a pointer that never was one) is refused with
+    EINVAL by every entry point instead of being dereferenced; destroying it
+    again is a no-op."""
+    import skinny_bf16_projection_gb300 as m
+    nat = m._native
+    lib = nat.lib()
+    w = torch.randn(256, 1024, device=DEV).to(torch.bfloat16)
+    x = torch.zeros(4, 1024, device=DEV, dtype=torch.bfloat16)
+    out = torch.zeros(4, 256, device=DEV, dtype=torch.bfloat16)
+    st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    h = lib.skinny_gemm_prepare(w.data_ptr(), 256, 1024, nat.SKG_BF16, nat.SKG_BF16)
+    assert h
+    assert lib.skinny_gemm_run(h, x.data_ptr(), 4, out.data_ptr(), st) == nat.SKG_OK
+    lib.skinny_gemm_destroy(h)
+    lib.skinny_gemm_destroy(h)  # second destroy: ignored
+    assert lib.skinny_gemm_run(h, x.data_ptr(), 4, out.data_ptr(), st) == nat.SKG_EINVAL
+    assert "destroyed" in nat.last_error()
+    buf = ctypes.create_string_buffer(64)
+    assert lib.skinny_gemm_plan_query(h, 4, buf, 64) == nat.SKG_EINVAL
+    foreign = ctypes.c_void_p(x.data_ptr())
+    assert lib.skinny_gemm_run(foreign, x.data_ptr(), 4, out.data_ptr(), st) == nat.SKG_EINVAL
+    torch.cuda.synchronize()
+
+
 def test_autotune_refuses_during_capture():
     import skinny_bf16_projection_gb300 as m
     nat = m._native
