@@ -1460,7 +1460,7 @@ extern "C" int skinny_gemm_run_noalloc(const void* W, int64_t N, int64_t K, int6
   p.kboxes = static_cast<int>((K + kBoxK - 1) / kBoxK);
   p.status = scratch;
   p.timeout_ns = env_u64("SKINNY_GEMM_TIMEOUT_NS", 2000000000ull);
-  int rc = validate_run(&p, x, ldx, M, out, ldo);
+  int rc = validate_args(&p, x, ldx, M, out, ldo);  // p is a private plan, not a handle
   if (rc != SKG_OK) return rc;
   const Tactic t = default_tactic(&p, M);
   if (!t.valid()) return fail(SKG_EINVAL, "no valid tactic for M = %lld", static_cast<long long>(M));
