@@ -1258,7 +1258,9 @@ int skinny_gemm_autotune(skinny_gemm_t h, const int64_t* Ms, int nM, void* strea
   for (int i = 0; i < nM && rc == SKG_OK; ++i) {
     const int64_t M = Ms[i];
     // Time one tactic as a graph of L back-to-back launches over the rotated copies.
-    auto time_tactic = [&](const Tactic& t, double* us_out) -> int {
+    auto time_tactic = [&](const Tactic& t, double* us_out, int nrep = 0, int mult = 1) -> int {
+      const int LL = L * mult;
+      const int RR = nrep > 0 ? nrep : reps;
       int trc = ensure_workspace(h, t);
       if (trc != SKG_OK) return trc;
       for (skinny_gemm_plan& sh : shadow) {
@@ -1271,7 +1273,7 @@ int skinny_gemm_autotune(skinny_gemm_t h, const int64_t* Ms, int nM, void* strea
       cudaGraphExec_t exec = nullptr;
       cudaError_t ce = cudaStreamBeginCapture(ts, cudaStreamCaptureModeThreadLocal);
       if (ce != cudaSuccess) return cuda_fail(ce, "cudaStreamBeginCapture(autotune)");
-      for (int l = 0; l < L && trc == SKG_OK; ++l)
+      for (int l = 0; l < LL && trc == SKG_OK; ++l)
         trc = launch_tactic(&shadow[l % R], t, xbuf, h->K, M, obuf, h->N, ts);
       ce = cudaStreamEndCapture(ts, &graph);
       if (trc != SKG_OK || ce != cudaSuccess) {
@@ -1285,7 +1287,7 @@ int skinny_gemm_autotune(skinny_gemm_t h, const int64_t* Ms, int nM, void* strea
       }
       float best_ms = 1e30f;
       ce = cudaGraphLaunch(exec, ts);  // warm-up
-      for (int r = 0; r < reps && ce == cudaSuccess; ++r) {
+      for (int r = 0; r < RR && ce == cudaSuccess; ++r) {
         cudaEventRecord(e0, ts);
         ce = cudaGraphLaunch(exec, ts);
         cudaEventRecord(e1, ts);
@@ -1299,7 +1301,7 @@ int skinny_gemm_autotune(skinny_gemm_t h, const int64_t* Ms, int nM, void* strea
       cudaGraphExecDestroy(exec);
       cudaGraphDestroy(graph);
       if (ce != cudaSuccess) return cuda_fail(ce, "autotune timing");
-      *us_out = 1000.0 * best_ms / L;
+      *us_out = 1000.0 * best_ms / LL;
       if (log_enabled())
         fprintf(stderr, "[skinny_gemm] tune N=%lld K=%lld M=%lld %s %.3f us\n",
                 static_cast<long long>(h->N), static_cast<long long>(h->K),
@@ -1329,6 +1331,19 @@ int skinny_gemm_autotune(skinny_gemm_t h, const int64_t* Ms, int nM, void* strea
           if (rc == SKG_OK) timed.push_back({us, t});
         }
       }
+    }
+    // Phase 3: the four fastest so far timed again, longer (twice the launches,
+    // five repetitions), so that near-ties are not decided by timing noise.
+    if (rc == SKG_OK && timed.size() > 1) {
+      std::stable_sort(timed.begin(), timed.end(),
+                       [](const auto& a, const auto& b) { return a.first < b.first; });
+      std::vector<std::pair<double, Tactic>> fin;
+      for (size_t c = 0; c < timed.size() && c < 4 && rc == SKG_OK; ++c) {
+        double us = 0;
+        rc = time_tactic(timed[c].second, &us, 5, 2);
+        if (rc == SKG_OK) fin.push_back({us, timed[c].second});
+      }
+      if (rc == SKG_OK) timed = fin;
     }
     double best_us = 1e30;
     Tactic best;
