@@ -278,7 +278,7 @@ int ntiles_of(const skinny_gemm_plan* h, const Tactic& t) {
 }
 uint32_t tactic_smem(const Tactic& t) {
   if (t.variant == kVariantSk) return sk_smem_bytes(t.tok, t.nbox, t.stages);
-  if (t.variant == kVariantTc) return tc_smem_bytes(t.tok, t.nbox, t.stages, t.cl, t.al != 0);
+  if (t.variant == kVariantTc) return tc_smem_bytes(t.tok, t.nbox, t.stages, t.cl, t.al != 0, t.rows);
   return smem_bytes(t.rows, t.tok, t.nbox, t.stages);
 }
 // CTAs launched: row tiles x cluster size, or (stream-K) CTAs-per-SM x SMs,
@@ -325,8 +325,10 @@ bool tactic_fits(const skinny_gemm_plan* h, const Tactic& t, int64_t M, std::str
     if (t.rows % t.cl != 0) return no("cluster size must divide the row tile");
   }
   if (t.stages < 1 || t.stages > 16) return no("stages out of range 1..16");
-  if (t.al && (t.cl < 2 || static_cast<uint32_t>(t.stages) * stage_bytes(128, t.tok, t.nbox) <
-                               tc_red_bytes(t.tok)))
+  if (t.variant == kVariantTc && t.rows / t.cl < 8)
+    return no("tcgen05 cluster reduction needs at least 8 rows per CTA (rows / cluster)");
+  if (t.al && (t.cl < 2 || static_cast<uint32_t>(t.stages) * stage_bytes(t.rows, t.tok, t.nbox) <
+                               tc_red_bytes(t.tok, t.rows)))
     return no("an aliased receive buffer needs a cluster and stages at least as large");
   if (static_cast<int>(tactic_smem(t)) > h->dev->smem_optin)
     return no("shared memory footprint exceeds the per-block limit");

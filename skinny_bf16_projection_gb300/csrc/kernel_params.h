@@ -76,15 +76,15 @@ const KernelEntry* sk_kernel_table(int* count);
 // tcgen05 cluster kernel: the receive buffer is [cluster][rows/cluster][TOK + 4]
 // fp32 (token-contiguous rows, padded so 16-byte reads of consecutive rows
 // fall in different banks).
-__host__ __device__ constexpr uint32_t tc_red_bytes(int tok) {
-  return static_cast<uint32_t>(128 * (tok + 4) * 4);
+__host__ __device__ constexpr uint32_t tc_red_bytes(int tok, int rows = 128) {
+  return static_cast<uint32_t>(rows * (tok + 4) * 4);
 }
 // (The receive buffer exists only for clusters of more than one CTA, and takes
 // no space of its own when it aliases the pipeline stages.)
 __host__ __device__ constexpr uint32_t tc_smem_bytes(int tok, int nbox, int stages, int cluster,
-                                                     bool alias = false) {
-  return kSmemAlign + stages * stage_bytes(128, tok, nbox) +
-         (cluster > 1 && !alias ? tc_red_bytes(tok) : 0u) +
+                                                     bool alias = false, int rows = 128) {
+  return kSmemAlign + stages * stage_bytes(rows, tok, nbox) +
+         (cluster > 1 && !alias ? tc_red_bytes(tok, rows) : 0u) +
          static_cast<uint32_t>((2 * stages + 4) * 8) + 16;
 }
 

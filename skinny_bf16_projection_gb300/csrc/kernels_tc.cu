@@ -30,18 +30,18 @@
 
 namespace skg {
 
-template <int TOK, int NBOX, typename OutT, bool kFp16>
+template <int TOK, int NBOX, typename OutT, bool kFp16, int ROWS = 128>
 __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ CUtensorMap wmap,
                                                       const __grid_constant__ CUtensorMap xmap,
                                                       const KParams p) {
-  constexpr int ROWS = 128;
   constexpr uint32_t kWBox = ROWS * kBoxRowBytes;
   constexpr uint32_t kXBox = TOK * kBoxRowBytes;
   constexpr uint32_t kStage = stage_bytes(ROWS, TOK, NBOX);
   constexpr uint32_t kTmemCols = TOK <= 32 ? 32u : static_cast<uint32_t>(TOK);
   constexpr uint32_t kIdesc = mma_idesc<kFp16>(ROWS, TOK);
   constexpr uint32_t kStageRed = static_cast<uint32_t>(ROWS * TOK) * 4u;
-  static_assert(TOK % 16 == 0 && TOK >= 16 && TOK <= 256, "M=128 MMA needs N % 16 == 0, N <= 256");
+  static_assert(TOK % 16 == 0 && TOK >= 16 && TOK <= 256, "MMA needs N % 16 == 0, N <= 256");
+  static_assert(ROWS == 128 || ROWS == 64, "MMA M is 128 or 64 weight rows");
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
   // the cluster barrier that each CTA arrives at from that point on.
   const bool alias = p.red_alias != 0 && csize > 1;
   const uint32_t stages_end = base + static_cast<uint32_t>(S) * kStage;
-  const uint32_t bars = stages_end + (csize > 1 && !alias ? tc_red_bytes(TOK) : 0u);
+  const uint32_t bars = stages_end + (csize > 1 && !alias ? tc_red_bytes(TOK, ROWS) : 0u);
   const uint32_t done_bar = bars + 8u * (2 * S);
   const uint32_t recv_bar = done_bar + 8u;
   const uint32_t dbg_bar = done_bar + 16u;
@@ -207,8 +207,12 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
   // The accumulator is read 32 TMEM columns (tokens) at a time, so registers
   // stay bounded for token tiles up to 256.
   constexpr int CH = TOK < 32 ? TOK : 32;
+  // Accumulator row r lives in TMEM lane r (M = 128) or, for M = 64, in lane
+  // 16 * (r / 16) + r (the first 16 lanes of each warp's quarter); warp w
+  // reads its own quarter, lanes 32w .. 32w + 31.
   const uint32_t row_taddr = tmem + ((warp * 32u) << 16);
-  const int r = static_cast<int>(warp * 32u + lane);
+  const bool row_ok = ROWS == 128 || lane < 16u;
+  const int r = ROWS == 128 ? static_cast<int>(warp * 32u + lane) : static_cast<int>(warp * 16u + (lane & 15u));
   auto load_chunk = [&](int c0, float (&v)[CH]) {
 #pragma unroll
     for (int c = 0; c < CH / 16; ++c) {
@@ -224,7 +228,7 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
     for (int c0 = 0; c0 < TOK && c0 < M; c0 += CH) {
       float v[CH];
       load_chunk(c0, v);
-      if (n < p.N) {
+      if (row_ok && n < p.N) {
 #pragma unroll
         for (int i = 0; i < CH; ++i)
           if (c0 + i < M) store_out<OutT>(p, m0 + c0 + i, n, v[i]);
@@ -245,7 +249,7 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
       load_chunk(c0, v);
 #pragma unroll
       for (int i = 0; i < CH; ++i)
-        if (c0 + i < M)
+        if (row_ok && c0 + i < M)
           asm volatile("st.shared.f32 [%0], %1;" ::"r"(dst + static_cast<uint32_t>((c0 + i) * RS) * 4u),
                        "f"(v[i])
                        : "memory");
@@ -317,7 +321,7 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
 #pragma unroll
       for (int g = 0; g < CH / 4; ++g) {
         const int gg = c0 / 4 + g;
-        if (gg >= MG) continue;
+        if (gg >= MG || !row_ok) continue;
         if (owner == rank)
           asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(red + row_off + gg * 16u),
                        "f"(v[4 * g]), "f"(v[4 * g + 1]), "f"(v[4 * g + 2]), "f"(v[4 * g + 3])
@@ -372,11 +376,21 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
   }
 }
 
-#define SKG_TC_ENTRY(TOK, NBOX, OUTT, OUTCODE, FP16)                                        \
+#define SKG_TC_ENTRY_R(ROWS, TOK, NBOX, OUTT, OUTCODE, FP16)                               \
   KernelEntry {                                                                             \
-    kVariantTc, 128, TOK, NBOX, FP16 ? 1 : 0, OUTCODE, 128,                                 \
-        reinterpret_cast<const void*>(&skinny_tc_kernel<TOK, NBOX, OUTT, FP16>)             \
+    kVariantTc, ROWS, TOK, NBOX, FP16 ? 1 : 0, OUTCODE, 128,                                \
+        reinterpret_cast<const void*>(&skinny_tc_kernel<TOK, NBOX, OUTT, FP16, ROWS>)       \
   }
+#define SKG_TC_ENTRY(TOK, NBOX, OUTT, OUTCODE, FP16) SKG_TC_ENTRY_R(128, TOK, NBOX, OUTT, OUTCODE, FP16)
+
+// 64-row tiles (MMA M = 64): twice the CTAs of a 128-row tiling for the same
+// cluster size, half the partial sums per CTA in the cluster reduction.
+#define SKG_TC_ROW64(OUTT, OUTCODE)                                                         \
+  SKG_TC_ENTRY_R(64, 16, 1, OUTT, OUTCODE, false), SKG_TC_ENTRY_R(64, 16, 2, OUTT, OUTCODE, false), \
+      SKG_TC_ENTRY_R(64, 16, 4, OUTT, OUTCODE, false),                                      \
+      SKG_TC_ENTRY_R(64, 32, 1, OUTT, OUTCODE, false), SKG_TC_ENTRY_R(64, 32, 2, OUTT, OUTCODE, false), \
+      SKG_TC_ENTRY_R(64, 32, 4, OUTT, OUTCODE, false),                                      \
+      SKG_TC_ENTRY_R(64, 64, 1, OUTT, OUTCODE, false), SKG_TC_ENTRY_R(64, 64, 2, OUTT, OUTCODE, false)
 
 #define SKG_TC_ROW(OUTT, OUTCODE)                                                           \
   SKG_TC_ENTRY(16, 1, OUTT, OUTCODE, false), SKG_TC_ENTRY(16, 2, OUTT, OUTCODE, false),     \
@@ -394,6 +408,7 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
       SKG_TC_ENTRY(128, 1, OUTT, OUTCODE, true), SKG_TC_ENTRY(256, 1, OUTT, OUTCODE, true)
 
 static const KernelEntry kTcTable[] = {SKG_TC_ROW(__nv_bfloat16, 0), SKG_TC_ROW(float, 2),
+                                       SKG_TC_ROW64(__nv_bfloat16, 0), SKG_TC_ROW64(float, 2),
                                        SKG_TC_ROW16(__half, 1), SKG_TC_ROW16(float, 2)};
 
 const KernelEntry* tc_kernel_table(int* count) {
