@@ -175,7 +175,7 @@ int skinny_gemm_run_overlap(skinny_gemm_t h_main, skinny_gemm_t h_fa, skinny_gem
  * timed as a CUDA graph of back-to-back launches that rotate over scratch
  * copies of the weight's layout (>= 4.5x the L2 size, so reads come from HBM),
  * i.e. in the steady state of a decode step; the fastest three are timed again
- * with later PDL triggers, and the fastest four with twice the launches and
+ * with later PDL triggers, and the fastest six with twice the launches and
  * five repetitions decide.  Synchronizes `stream`;
  * allocates and frees those copies; may grow the handle's workspace; writes
  * nothing the caller owns.  Must not be called while capturing (ECAPTURING).

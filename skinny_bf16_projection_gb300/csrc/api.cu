@@ -1334,13 +1334,13 @@ int skinny_gemm_autotune(skinny_gemm_t h, const int64_t* Ms, int nM, void* strea
         }
       }
     }
-    // Phase 3: the four fastest so far timed again, longer (twice the launches,
+    // Phase 3: the six fastest so far timed again, longer (twice the launches,
     // five repetitions), so that near-ties are not decided by timing noise.
     if (rc == SKG_OK && timed.size() > 1) {
       std::stable_sort(timed.begin(), timed.end(),
                        [](const auto& a, const auto& b) { return a.first < b.first; });
       std::vector<std::pair<double, Tactic>> fin;
-      for (size_t c = 0; c < timed.size() && c < 4 && rc == SKG_OK; ++c) {
+      for (size_t c = 0; c < timed.size() && c < 6 && rc == SKG_OK; ++c) {
         double us = 0;
         rc = time_tactic(timed[c].second, &us, 5, 2);
         if (rc == SKG_OK) fin.push_back({us, timed[c].second});
