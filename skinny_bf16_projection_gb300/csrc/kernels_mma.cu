@@ -260,6 +260,7 @@ __global__ void __launch_bounds__(160) skinny_mma_kernel(const __grid_constant__
 
 #define SKG_MMA_ROW(MT, OUTT, OUTCODE)                                                       \
   SKG_MMA_ENTRY(MT, 8, 1, OUTT, OUTCODE, false), SKG_MMA_ENTRY(MT, 16, 1, OUTT, OUTCODE, false), \
+      SKG_MMA_ENTRY(MT, 32, 1, OUTT, OUTCODE, false),                                       \
       SKG_MMA_ENTRY(MT, 8, 2, OUTT, OUTCODE, false), SKG_MMA_ENTRY(MT, 8, 4, OUTT, OUTCODE, false), \
       SKG_MMA_ENTRY(MT, 16, 2, OUTT, OUTCODE, false),                                        \
       SKG_MMA_ENTRY(MT, 16, 4, OUTT, OUTCODE, false),                                        \
