@@ -176,7 +176,9 @@ int skinny_gemm_run_overlap(skinny_gemm_t h_main, skinny_gemm_t h_fa, skinny_gem
  * copies of the weight's layout (>= 4.5x the L2 size, so reads come from HBM),
  * i.e. in the steady state of a decode step; the fastest three are timed again
  * with later PDL triggers, and the fastest six with twice the launches and
- * five repetitions decide.  Synchronizes `stream`;
+ * five repetitions decide.  Listed M values with the same candidate list (the
+ * same token tiles, e.g. M = 1..8) are tuned together and get one tactic.
+ * Synchronizes `stream`;
  * allocates and frees those copies; may grow the handle's workspace; writes
  * nothing the caller owns.  Must not be called while capturing (ECAPTURING).
  * When SKINNY_GEMM_TACTIC_FILE names a file, results are appended there and

@@ -1257,8 +1257,27 @@ int skinny_gemm_autotune(skinny_gemm_t h, const int64_t* Ms, int nM, void* strea
   }
   int rc = SKG_OK;
   std::vector<int64_t> tuned;
-  for (int i = 0; i < nM && rc == SKG_OK; ++i) {
-    const int64_t M = Ms[i];
+  // Token counts with identical candidate lists (the same token tiles) are tuned
+  // together: phases 1-2 at the largest of them, phase 3 summed over all of them,
+  // one tactic installed for the group (the same kernel for, e.g., M = 1..8).
+  std::vector<std::string> group_keys;
+  std::vector<std::vector<int64_t>> groups;
+  for (int i = 0; i < nM; ++i) {
+    std::string key;
+    for (const Tactic& t : candidates(h, Ms[i])) key += tactic_str(t) + ";";
+    size_t g = 0;
+    while (g < group_keys.size() && group_keys[g] != key) ++g;
+    if (g == group_keys.size()) {
+      group_keys.push_back(key);
+      groups.emplace_back();
+    }
+    if (std::find(groups[g].begin(), groups[g].end(), Ms[i]) == groups[g].end())
+      groups[g].push_back(Ms[i]);
+  }
+  for (size_t gi = 0; gi < groups.size() && rc == SKG_OK; ++gi) {
+    const std::vector<int64_t>& grp = groups[gi];
+    const int64_t Mmax = *std::max_element(grp.begin(), grp.end());
+    int64_t M = Mmax;  // token count the next timing runs at
     // Time one tactic as a graph of L back-to-back launches over the rotated copies.
     auto time_tactic = [&](const Tactic& t, double* us_out, int nrep = 0, int mult = 1) -> int {
       const int LL = L * mult;
@@ -1335,15 +1354,26 @@ int skinny_gemm_autotune(skinny_gemm_t h, const int64_t* Ms, int nM, void* strea
       }
     }
     // Phase 3: the six fastest so far timed again, longer (twice the launches,
-    // five repetitions), so that near-ties are not decided by timing noise.
-    if (rc == SKG_OK && timed.size() > 1) {
+    // five repetitions) and at every token count of the group (times summed), so
+    // that near-ties are not decided by timing noise.
+    if (rc == SKG_OK && (timed.size() > 1 || grp.size() > 1)) {
       std::stable_sort(timed.begin(), timed.end(),
                        [](const auto& a, const auto& b) { return a.first < b.first; });
       std::vector<std::pair<double, Tactic>> fin;
       for (size_t c = 0; c < timed.size() && c < 6 && rc == SKG_OK; ++c) {
-        double us = 0;
-        rc = time_tactic(timed[c].second, &us, 5, 2);
-        if (rc == SKG_OK) fin.push_back({us, timed[c].second});
+        double sum = 0;
+        for (size_t k = 0; k < grp.size() && rc == SKG_OK; ++k) {
+          if (!tactic_fits(h, timed[c].second, grp[k], nullptr)) {
+            sum = 1e30;
+            break;
+          }
+          M = grp[k];
+          double us = 0;
+          rc = time_tactic(timed[c].second, &us, 5, 2);
+          sum += us;
+        }
+        M = Mmax;
+        if (rc == SKG_OK) fin.push_back({sum / static_cast<double>(grp.size()), timed[c].second});
       }
       if (rc == SKG_OK) timed = fin;
     }
@@ -1354,10 +1384,12 @@ int skinny_gemm_autotune(skinny_gemm_t h, const int64_t* Ms, int nM, void* strea
         best_us = ut.first;
         best = ut.second;
       }
-    if (rc == SKG_OK && best.valid()) {
-      h->plan[M] = best;
-      tuned.push_back(M);
-      append_tactic_file(h, M, best, best_us);
+    if (rc == SKG_OK && best.valid() && best_us < 1e29) {
+      for (int64_t m : grp) {
+        h->plan[m] = best;
+        tuned.push_back(m);
+        append_tactic_file(h, m, best, best_us);
+      }
     }
   }
   cleanup();
