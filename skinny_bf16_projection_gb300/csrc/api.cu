@@ -558,12 +558,14 @@ std::vector<Tactic> candidates(const skinny_gemm_plan* h, int64_t M) {
 
 // Default (untuned) choice, from what the autotuner picked on GB300 for the
 // 3584x7168 and 6288x7168 weights with every weight read from HBM:
-//   M <= 8   mma.sync, 128-row tiles, 8-token tile, 2 boxes x 3 stages
+//   M <= 8   mma.sync, 128-row tiles, 8-token tile, 1 box x 2 stages with a
+//            16-way cluster where that keeps <= 3 CTAs/SM, else 2 boxes x 3 stages
 //   M <= 16  mma.sync, 64-row tiles, 16-token tile, 2 boxes x 2 stages
 //   M <= 32  tcgen05, 32-token tile, 2 boxes x 2 stages
 //   M <= 64  tcgen05, 64-token tile, 1 box x 3 stages
 // with the cluster split (split-K factor) that gives about 1.4 CTAs per SM
-// (64-row tiles: at most 3), at most 8; fewer stages where shared memory or
+// (64-row tiles and the one-box 8-token tiles: the largest giving at most 3),
+// at most 8 (16 for the latter); fewer stages where shared memory or
 // the K range is short, or where the grid would not be resident in one wave
 // (then 3 -> 2 stages, then half the cluster: e.g. the 6288x7168 weight runs
 // 2 stages for its 8-token tile and clusters of 4 for its 32/64-token tiles).  Any
@@ -577,7 +579,8 @@ Tactic default_tactic(const skinny_gemm_plan* h, int64_t M) {
     const int ntiles = static_cast<int>((h->N + t.rows - 1) / t.rows);
     const int sms = h->dev->sm_count;
     int cl = 1;
-    while (cl < 8 && cl * 2 <= h->kboxes && t.rows % (cl * 2) == 0 &&
+    const int cl_max = cap3 && t.nbox == 1 ? 16 : 8;
+    while (cl < cl_max && cl * 2 <= h->kboxes && t.rows % (cl * 2) == 0 &&
            (cap3 ? ntiles * cl * 2 <= 3 * sms : ntiles * cl * 10 < sms * 14))
       cl *= 2;
     t.cl = cl;
@@ -603,8 +606,13 @@ Tactic default_tactic(const skinny_gemm_plan* h, int64_t M) {
     return fit;
   };
   Tactic t;
-  if (M <= 8)
-    t = with_cluster(Tactic{kVariantMma, 128, 8, 2, 3, 1, 0});
+  if (M <= 8) {
+    // one-box stages pay off with 16-way clusters (measured on 3584x7168: 9.4 us
+    // vs 9.6); where the weight has too many row tiles for that (6288x7168) the
+    // two-box stages with a 1.4 CTAs/SM cluster stay ahead.
+    t = with_cluster(Tactic{kVariantMma, 128, 8, 1, 2, 1, 0}, true);
+    if (!t.valid() || t.cl < 16) t = with_cluster(Tactic{kVariantMma, 128, 8, 2, 3, 1, 0});
+  }
   else if (M <= 16)
     t = with_cluster(Tactic{kVariantMma, 64, 16, 2, 2, 1, 0}, true);
   else if (M <= 32)
