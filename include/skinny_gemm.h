@@ -216,6 +216,12 @@ int skinny_gemm_autotune_overlap(skinny_gemm_t h_main, skinny_gemm_t h_fa, skinn
  * parse or the tactic does not fit this weight and M. */
 int skinny_gemm_set_tactic(skinny_gemm_t h, int64_t M, const char* tactic);
 
+/* Parse a tactic string (grammar at skinny_gemm_set_tactic) and write its
+ * canonical spelling into buf (NUL-terminated, truncated to len): suffixes in
+ * the order ":d<k>", ":a".  No handle and no device needed.  EINVAL if it does
+ * not parse. */
+int skinny_gemm_tactic_normalize(const char* tactic, char* buf, size_t len);
+
 /* Write the tactic the plan uses for M into buf (NUL-terminated, truncated to
  * len).  Returns SKG_OK, or EINVAL/EUNSUPPORTED_M. */
 int skinny_gemm_plan_query(skinny_gemm_t h, int64_t M, char* buf, size_t len);

@@ -35,6 +35,7 @@ SIGNATURES = [
     ("skinny_gemm_autotune", _int, [_vp, ctypes.POINTER(_i64), _int, _vp]),
     ("skinny_gemm_autotune_overlap", _int, [_vp, _vp, _vp, _int, ctypes.POINTER(_i64), _int, _vp]),
     ("skinny_gemm_set_tactic", _int, [_vp, _i64, _cp]),
+    ("skinny_gemm_tactic_normalize", _int, [_cp, _cp, _sz]),
     ("skinny_gemm_plan_query", _int, [_vp, _i64, _cp, _sz]),
     ("skinny_gemm_list_tactics", _int, [_vp, _i64, _cp, _sz]),
     ("skinny_gemm_check_status", _int, [_vp, _vp]),

@@ -1156,6 +1156,14 @@ int skinny_gemm_autotune_overlap(skinny_gemm_t h_main, skinny_gemm_t h_fa, skinn
   return ok();
 }
 
+int skinny_gemm_tactic_normalize(const char* tactic, char* buf, size_t len) {
+  if (buf == nullptr || len == 0) return fail(SKG_EINVAL, "null buffer");
+  Tactic t;
+  if (!tactic_parse(tactic, &t)) return fail(SKG_EINVAL, "cannot parse tactic '%s'", tactic ? tactic : "");
+  snprintf(buf, len, "%s", tactic_str(t).c_str());
+  return ok();
+}
+
 int skinny_gemm_set_tactic(skinny_gemm_t h, int64_t M, const char* tactic) {
   if (check_handle(h) != SKG_OK) return SKG_EINVAL;
   if (M < 1 || M > SKINNY_GEMM_MAX_M)

@@ -71,3 +71,26 @@ def test_kernel_sources_use_blackwell_primitives():
                    "cp.async.bulk.tensor.2d", "L2::evict_first", "griddepcontrol.wait",
                    "st.async.shared::cluster", "mapa.shared::cluster"):
         assert needle in text, needle
+
+
+def test_tactic_grammar_without_a_gpu(lib_path):
+    """The tactic strings accepted by skinny_gemm_set_tactic, parsed without a
+    handle: canonical spellings round-trip, suffixes are order-free, and
+    malformed strings are refused."""
+    from skinny_bf16_projection_gb300 import _native
+    lib = _native.load(lib_path)
+    buf = ctypes.create_string_buffer(96)
+
+    def norm(t):
+        rc = lib.skinny_gemm_tactic_normalize(t.encode(), buf, 96)
+        return buf.value.decode() if rc == _native.SKG_OK else rc
+
+    for t in ("mma:r128:t8:b2:s3:c8", "mma:r64:t16:b1:s2:c16:d3", "tc:r128:t32:b2:s2:c8:d1",
+              "tc:r64:t64:b2:s2:c4:d2:a", "tc:r128:t128:b1:s3:c4:a", "sk:r128:t16:b2:s3:p8",
+              "sk:r128:t32:b1:s4:g2"):
+        assert norm(t) == t
+    assert norm("tc:r128:t64:b2:s2:c8:a:d1") == "tc:r128:t64:b2:s2:c8:d1:a"  # order-free
+    for bad in ("bogus", "tc:r128:t32:b2:s2", "tc:r128:t32:b2:s2:c8:x", "tc:r128:t32:b2:s2:c8:d0",
+                "tc:r128:t32:b2:s2:c8:d1:d2", "tc:r128:t32:b2:s2:c8:a:a", "mma:r128:t8:b2:s2:c8:a",
+                "sk:r128:t16:b2:s3:p8:d1", "tc:r128:t32:b2:s2:g1", "mma:r128:t8:b2:s2:c8:ab"):
+        assert norm(bad) == _native.SKG_EINVAL, bad
