@@ -1,15 +1,17 @@
 """Benchmark: skinny BF16 decode projection on GB300.
 
 Workload (default): the decode projection W[3584, 7168] bf16, one sweep of
-M = 1, 2, 4, 8, 16, 32 tokens per step (six projections, bf16 output), inputs
-resident in HBM.  Each projection reads a different copy of the weight from a
-rotation of R copies whose total is >= 4.5x the L2 size, so every weight read
-comes from HBM.  Prints one JSON line (rank 0).
+M = 1, 2, 4, 8, 16, 32, 48, 64 tokens per step (eight projections, bf16
+output), inputs resident in HBM.  Each projection reads a different copy of the
+weight from a rotation of R copies whose total is >= 4.5x the L2 size, so every
+weight read comes from HBM.  A timed window is exactly K steps (one CUDA graph
+replay); windows are repeated for about a second and the median window gives
+the step time.  Prints one JSON line (rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
 Under torchrun each rank runs an independent replica on its own GPU (the
-projection has no exchange step); the step time is the max over ranks.
+projection has no exchange step); each window's time is the max over ranks.
 """
 from __future__ import annotations
 
@@ -31,7 +33,16 @@ if ROOT not in sys.path:
 
 METRIC = "us per projection and weight-stream HBM GB/s (% of GB300 peak) at M=1..64"
 N_DEC, K_DEC = 3584, 7168
-SWEEP = (1, 2, 4, 8, 16, 32)
+SWEEP = (1, 2, 4, 8, 16, 32, 48, 64)
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e nominal, beside the measured copy peak
+
+
+def workload_config(world: int) -> dict:
+    """The `config` of the JSON line, identical for both arms."""
+    return {"workload": f"decode projection W[{N_DEC},{K_DEC}] bf16, sweep M={list(SWEEP)} "
+                        f"({len(SWEEP)} projections per step), bf16 out",
+            "N": N_DEC, "K": K_DEC, "M": list(SWEEP), "out": "bf16",
+            "parallelism": f"replicas x{world}"}
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -45,7 +56,7 @@ def measured_peaks() -> dict:
 
 
 # Source files of the decode sweep's dominant kernel (the mma.sync kernel that runs
-# M <= 16): the recorded DRAM traffic stays valid while these are unchanged.
+# M <= 8): the recorded DRAM traffic stays valid while these are unchanged.
 DOMINANT_SOURCES = ("kernels_mma.cu", "device_common.cuh", "kernel_params.h")
 
 
@@ -151,6 +162,17 @@ def reduce_max(value: float, world: int) -> float:
     return float(t.item())
 
 
+def reduce_max_windows(win_ms: list[float], world: int) -> list[float]:
+    """Each timed window's duration as the slowest rank saw it."""
+    if world == 1:
+        return list(win_ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(win_ms, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 def barrier(world: int):
     if world > 1:
         import torch.distributed as dist
@@ -230,9 +252,9 @@ def cpu_model() -> str:
 # ----------------------------------------------------------------------------- reference arm
 def reference_arm(args, rank, world):
     """The oracle timed as it stands on the host cores.  One step = one sweep of
-    M = 1..32 over a row sample of the weight, sized so that warm-up + K steps
-    take about 90 s; throughput is scaled to weight bytes (rows * K * 2 per
-    projection)."""
+    the headline token counts over a row sample of the weight, sized so that
+    warm-up + K steps take about 90 s; throughput is scaled to weight bytes
+    (rows * K * 2 per projection)."""
     if rank != 0:
         return 0
     import oracle
@@ -272,10 +294,7 @@ def reference_arm(args, rank, world):
         "ms_per_step": round(per_step * 1e3 * N_DEC / rows, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded randn, bf16 inputs)",
-        "config": {"workload": f"decode projection W[{N_DEC},{K_DEC}] bf16, sweep M={list(SWEEP)} "
-                               f"(6 projections per step), bf16 out",
-                   "N": N_DEC, "K": K_DEC, "M": list(SWEEP), "out": "bf16",
-                   "parallelism": "replicas"},
+        "config": workload_config(world),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -355,7 +374,7 @@ def other_workloads(torch, skg, pin, dev, l2, peak_gbs):
             entry[f"M{M}_bf16_same_weight_L2_assisted"] = {"us": round(us, 3),
                                                            "weight_GBps": round(wbytes / us / 1e3, 1)}
         # context only (not part of this library): cuBLAS through torch.mm, same rotation
-        for M in (1, 8, 32, 64, 128, 256):
+        for M in (1, 8, 16, 32, 48, 64, 128, 256):
             out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
             xm = xd[:M].contiguous()
             us = graph_time_us(torch, stream, dev,
@@ -509,19 +528,61 @@ def dependent_chain(torch, skg, pin, dev, l2, peak_gbs):
 
 
 # ----------------------------------------------------------------------------- our arm
+def rotation_copies(r_min: int, launches_per_window: int) -> tuple[int, bool]:
+    """Weight copies R >= r_min for the rotation.  When R divides the launches of
+    one timed window, window after window continues the rotation without a
+    repeat, so windows can run back to back; otherwise the L2 is flushed
+    between windows (outside the timed region).  Returns (R, flush)."""
+    for r in range(r_min, 4 * r_min + 1):
+        if launches_per_window % r == 0:
+            return r, False
+    return r_min, True
+
+
+def host_call_cost(torch, skg, proj, x, out, stream, calls: int = 10000, burst: int = 200):
+    """Host microseconds per eager call, enqueue time only: bursts of `burst`
+    calls (well below the launch queue depth, so no call waits for the GPU),
+    each burst timed with perf_counter and followed by a synchronize.  Through
+    the Python binding (Projection.run: shape checks + ctypes) and through the
+    bare C-ABI call (ctypes with prepared arguments)."""
+    lib = skg._native.lib()
+    h = proj._h
+    xp, op = x.data_ptr(), out.data_ptr()
+    M = x.shape[0]
+    sp = __import__("ctypes").c_void_p(stream.cuda_stream)
+    res = {}
+    for name, fn in (("python_run_us", lambda: proj.run(x, out, stream)),
+                     ("c_abi_run_us", lambda: lib.skinny_gemm_run(h, xp, M, op, sp))):
+        fn()
+        torch.cuda.synchronize()
+        total, n = 0.0, 0
+        while n < calls:
+            t0 = time.perf_counter()
+            for _ in range(burst):
+                fn()
+            total += time.perf_counter() - t0
+            n += burst
+            torch.cuda.synchronize()
+        res[name] = round(total / n * 1e6, 3)
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-tune", action="store_true", help="use the default plan")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--timed-seconds", type=float, default=1.5,
+                    help="repeat the K-step timed window for about this long (median reported)")
     ap.add_argument("--no-other-workloads", action="store_true",
-                    help="skip the per-config table (6288x7168, token tiles 48/64, fp32, overlap)")
+                    help="skip the per-config table (6288x7168, fp32, overlap, residual, ...)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    args.steps = max(args.steps, 1)
     rank, world, local = dist_setup()
     if args.impl == "reference":
         return reference_arm(args, rank, world)
@@ -537,8 +598,9 @@ def main():
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 128 << 20))
     wbytes = N_DEC * K_DEC * 2
+    n_launch = len(SWEEP)
     # >= 4.5x L2 of rotated copies: a cyclic read of ~2x L2 was measured still partly L2-fed
-    R = max(12, math.ceil(4.5 * l2 / wbytes))
+    R, flush = rotation_copies(max(12, math.ceil(4.5 * l2 / wbytes)), args.steps * n_launch)
 
     w, x = pin.case(N_DEC, K_DEC, seed=0)
     wd = w.to(dev)
@@ -554,112 +616,120 @@ def main():
     xs = {M: xd[:M].contiguous() for M in SWEEP}
     outs = {M: torch.empty((M, N_DEC), dtype=torch.bfloat16, device=dev) for M in SWEEP}
     stream = torch.cuda.current_stream(dev)
-    launches_per_step = len(SWEEP)
+    flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device=dev) if flush else None
 
-    # Each step is 6 launches; launch L reads weight copy L % R.  Steps are
-    # captured in CUDA graphs of G steps (6G % R == 0, so every graph starts at
-    # copy 0) and replayed; a remainder graph makes the count exactly K steps.
-    G = R * max(1, math.ceil(48 / R))
-
-    def capture(n_steps: int, fn):
+    def capture(n_launches: int, fn):
+        """One CUDA graph of fn's launches (captured on a side stream)."""
         g = torch.cuda.CUDAGraph()
         side = torch.cuda.Stream(dev)
         side.wait_stream(stream)
         with torch.cuda.graph(g, stream=side):
-            fn(n_steps)
+            fn(n_launches)
         stream.wait_stream(side)
         return g
 
-    def sweep_steps(n_steps: int):
-        c = 0
-        for _ in range(n_steps):
-            for M in SWEEP:
-                projs[c % R].run(xs[M], outs[M])
-                c += 1
+    def sweep_launches(n: int):
+        for c in range(n):
+            M = SWEEP[c % n_launch]
+            projs[c % R].run(xs[M], outs[M])
 
-    g_main = capture(G, sweep_steps)
-    rem = args.steps % G
-    g_rem = capture(rem, sweep_steps) if rem else None
+    # Timed window = exactly K steps = one replay of this graph (K * 8 launches,
+    # launch c reads weight copy c % R).
+    g_win = capture(args.steps * n_launch, sweep_launches)
 
-    # ---------------- timed region: exactly K steps, events on the launching stream
+    # ---------------- timed region: K-step windows, events on the launching stream
     sampler = ClockSampler(getattr(props, "uuid", None) and str(props.uuid))
     sampler.start()
     time.sleep(0.3)
-    for _ in range(max(1, math.ceil(args.warmup / G))):
-        g_main.replay()
+    for _ in range(max(1, math.ceil(args.warmup / args.steps))):  # >= W warm-up steps
+        g_win.replay()
     torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    g_win.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    est_ms = max(a.elapsed_time(b), 1e-3)
+    n_win = int(min(5000, max(15, math.ceil(args.timed_seconds * 1e3 / est_ms))))
+    n_win = int(reduce_max(float(n_win), world))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n_win)]
+    for e0, e1 in evs:
+        if flush:
+            flush_buf.fill_(1)
+        barrier(world)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        g_win.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
     barrier(world)
-    torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(args.steps // G):
-        g_main.replay()
-    if g_rem is not None:
-        g_rem.replay()
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    ms_total = ev0.elapsed_time(ev1)
     clocks = sampler.stop()
+    win_sorted = sorted(reduce_max_windows([e0.elapsed_time(e1) for e0, e1 in evs], world))
+    ms_step = statistics.median(win_sorted) / args.steps
     for p in projs:
         p.check_status()
-    ms_total = reduce_max(ms_total, world)
-    ms_step = ms_total / args.steps
-    value = world * launches_per_step * wbytes / (ms_step * 1e-3) / 1e9  # weight GB/s, all ranks
+    value = world * n_launch * wbytes / (ms_step * 1e-3) / 1e9  # weight GB/s, all ranks
 
-    # ---------------- per-M projection time (graph of 6R launches of one M, rotated)
+    # ---------------- per-M projection time (graph of R * 4 launches of one M, rotated)
+    peaks = measured_peaks()
     per_m = {}
     for M in SWEEP:
         def one_m(n, M=M):
             for i in range(n):
                 projs[i % R].run(xs[M], outs[M])
-        gm = capture(6 * R * 4, one_m)
+        gm = capture(R * max(4, math.ceil(96 / R)), one_m)
+        nl = R * max(4, math.ceil(96 / R))
         gm.replay()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         reps = 20
         a.record(stream)
         for _ in range(reps):
             gm.replay()
         b.record(stream)
         torch.cuda.synchronize()
-        us = a.elapsed_time(b) * 1e3 / (reps * 6 * R * 4)
-        per_m[str(M)] = {"us": round(us, 3), "weight_GBps": round(wbytes / us / 1e3, 1),
+        us = a.elapsed_time(b) * 1e3 / (reps * nl)
+        gbs = wbytes / us / 1e3
+        per_m[str(M)] = {"us": round(us, 3), "weight_GBps": round(gbs, 1),
+                         "frac": round(gbs / peaks["hbm_gbs"], 4),
+                         "frac_of_nominal_8TBps": round(gbs / NOMINAL_HBM_GBS, 4),
                          "tactic": plan[M]}
         del gm
 
+    # ---------------- host cost per eager call (enqueue only; no GPU wait in the bursts)
+    host_us = host_call_cost(torch, skg, projs[0], xs[1], outs[1], stream)
+
     # ---------------- end to end: C-ABI calls with pinned host buffers, copies inside.
-    # One step = the sweep's 6 projections, each copying its x in and its out back
+    # One step = the sweep's projections, each copying its x in and its out back
     # (skinny_gemm_run_host_async), each on its own stream so one projection's copies
     # overlap another's kernel, joined with events, then one synchronize per step.
     xh = {M: x[:M].contiguous().pin_memory() for M in SWEEP}
     oh = {M: torch.empty((M, N_DEC), dtype=torch.bfloat16).pin_memory() for M in SWEEP}
     e2e_steps = 200
-    n_str = 6
-    e2e_streams = [torch.cuda.Stream(dev) for _ in range(n_str)]
+    e2e_streams = [torch.cuda.Stream(dev) for _ in range(n_launch)]
     fork_ev = torch.cuda.Event()
-    join_evs = [torch.cuda.Event() for _ in range(n_str)]
+    join_evs = [torch.cuda.Event() for _ in range(n_launch)]
 
     def e2e_step(base: int, root):
         fork_ev.record(root)
         for st in e2e_streams:
             st.wait_event(fork_ev)
         for j, M in enumerate(SWEEP):
-            projs[(base + j) % R].run_host_async(xh[M], oh[M], e2e_streams[j % n_str])
+            projs[(base + j) % R].run_host_async(xh[M], oh[M], e2e_streams[j])
         for st, ev in zip(e2e_streams, join_evs):
             ev.record(st)
             root.wait_event(ev)
 
     root = torch.cuda.current_stream(dev)
     for g in range(2):
-        e2e_step(g * len(SWEEP), root)
+        e2e_step(g * n_launch, root)
     torch.cuda.synchronize()
     barrier(world)
     t0 = time.perf_counter()
     for i in range(e2e_steps):
-        e2e_step((i % 2) * len(SWEEP), root)
+        e2e_step((i % 2) * n_launch, root)
         root.synchronize()
     e2e_s = reduce_max(time.perf_counter() - t0, world) / e2e_steps
-    e2e_eager = world * launches_per_step * wbytes / e2e_s / 1e9
+    e2e_eager = world * n_launch * wbytes / e2e_s / 1e9
     # The same step captured as a CUDA graph per set of handles (the calls are
     # capturable: pinned-memory copies become graph nodes that run on every
     # replay), replayed with one synchronize per step.
@@ -669,7 +739,7 @@ def main():
     for g in range(2):
         gr = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gr, stream=side):
-            e2e_step(g * len(SWEEP), side)
+            e2e_step(g * n_launch, side)
         e2e_graphs.append(gr)
     for gr in e2e_graphs:
         gr.replay()
@@ -680,13 +750,13 @@ def main():
         e2e_graphs[i % 2].replay()
         root.synchronize()
     e2e_s = reduce_max(time.perf_counter() - t0, world) / e2e_steps
-    e2e_async = world * launches_per_step * wbytes / e2e_s / 1e9
+    e2e_async = world * n_launch * wbytes / e2e_s / 1e9
     # The same step with the copies batched around the projections on one stream:
-    # the six x (packed in one pinned host buffer, one row block per projection) copied
-    # in with one copy, the six skinny_gemm_run calls back to back (so programmatic
-    # dependent launch overlaps them as in a decode step), the six outputs (one packed
-    # device buffer) copied back with one copy; one CUDA graph per set of handles, one
-    # synchronize.  Same bytes each way as above.
+    # every x (packed in one pinned host buffer, one row block per projection) copied
+    # in with one copy, the skinny_gemm_run calls back to back (so programmatic
+    # dependent launch overlaps them as in a decode step), the outputs (one packed
+    # device buffer) copied back with one copy; one CUDA graph per set of handles,
+    # one synchronize.  Same bytes each way as above.
     rows = sum(SWEEP)
     offs, o = {}, 0
     for M in SWEEP:
@@ -710,7 +780,7 @@ def main():
     for g in range(2):
         gr = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gr, stream=side):
-            batched_step(g * len(SWEEP), side)
+            batched_step(g * n_launch, side)
         b_graphs.append(gr)
     for gr in b_graphs:
         gr.replay()
@@ -721,38 +791,52 @@ def main():
         b_graphs[i % 2].replay()
         root.synchronize()
     e2e_s = reduce_max(time.perf_counter() - t0, world) / e2e_steps
-    e2e_batched = world * launches_per_step * wbytes / e2e_s / 1e9
+    e2e_batched = world * n_launch * wbytes / e2e_s / 1e9
     e2e_value = max(e2e_batched, e2e_async)
-    e2e_method = ("per step: the six x copied in with one copy from pinned host memory, six "
-                  "skinny_gemm_run calls back to back, the six outputs copied back with one "
-                  "copy, one CUDA graph, one synchronize" if e2e_batched >= e2e_async else
-                  "per step: 6 skinny_gemm_run_host_async calls (pinned x in, out back) on 6 "
-                  "streams joined by events, captured in a CUDA graph, replayed, one synchronize")
+    e2e_method = ("per step: every x copied in with one copy from pinned host memory, the "
+                  "skinny_gemm_run calls back to back, the outputs copied back with one copy, "
+                  "one CUDA graph, one synchronize" if e2e_batched >= e2e_async else
+                  f"per step: {n_launch} skinny_gemm_run_host_async calls (pinned x in, out back) "
+                  f"on {n_launch} streams joined by events, captured in a CUDA graph, replayed, "
+                  "one synchronize")
 
-    # ---------------- roofline of the projection kernel (the only kernel in the step)
-    peaks = measured_peaks()
-    alg_bytes = sum(wbytes + M * K_DEC * 2 + M * N_DEC * 2 for M in SWEEP) / len(SWEEP)
-    avg_launch_s = ms_step * 1e-3 / launches_per_step
+    # ---------------- roofline of the projection kernels (the only kernels in the step)
+    alg_bytes = sum(wbytes + M * K_DEC * 2 + M * N_DEC * 2 for M in SWEEP) / n_launch
+    avg_launch_s = ms_step * 1e-3 / n_launch
     achieved = alg_bytes / avg_launch_s / 1e9
     traffic = recorded_traffic("decode_3584x7168_sweep")
+    dom = [str(M) for M in SWEEP if M <= 8]
+    dom_us = statistics.mean(per_m[m]["us"] for m in dom)
+    dom_alg = statistics.mean(wbytes + int(m) * K_DEC * 2 + int(m) * N_DEC * 2 for m in dom)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded randn, bf16 inputs, random weights)",
-        "config": {"workload": f"decode projection W[{N_DEC},{K_DEC}] bf16, sweep M={list(SWEEP)} "
-                               f"(6 projections per step), bf16 out",
-                   "N": N_DEC, "K": K_DEC, "M": list(SWEEP), "out": "bf16",
-                   "l2": f"rotating {R} weight copies ({R * wbytes / 1e6:.0f} MB >= 4.5x L2 "
-                         f"{l2 / 1e6:.0f} MB): every weight read comes from HBM",
-                   "parallelism": f"replicas x{world}"},
-        "us_per_projection": round(ms_step * 1e3 / launches_per_step, 3),
+        "config": workload_config(world),
+        "timing": {"windows": n_win, "steps_per_window": args.steps,
+                   "launches_per_window": args.steps * n_launch,
+                   "window_ms_p10_median_p90": [round(win_sorted[len(win_sorted) // 10], 4),
+                                                round(statistics.median(win_sorted), 4),
+                                                round(win_sorted[(9 * len(win_sorted)) // 10], 4)],
+                   "l2": (f"rotating {R} weight copies ({R * wbytes / 1e6:.0f} MB >= 4.5x L2 "
+                          f"{l2 / 1e6:.0f} MB): every weight read comes from HBM; "
+                          + ("L2 flushed between windows" if flush else
+                             "windows back to back (R divides the launches of a window)"))},
+        "us_per_projection": round(ms_step * 1e3 / n_launch, 3),
         "per_M": per_m,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "frac_of_nominal_8TBps": round(achieved / NOMINAL_HBM_GBS, 4),
                      "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs, burst copy)",
-                     "traffic": traffic},
+                     "kernel": "the projection kernels: every launch of the step (algorithmic "
+                               "bytes per launch averaged over the sweep / step time per launch)",
+                     "traffic": traffic,
+                     "dominant": {"kernel": f"M<=8 tactic {plan[1]} ({len(dom)} of {n_launch} "
+                                            f"launches)",
+                                  "achieved": round(dom_alg / dom_us / 1e3, 1),
+                                  "frac": round(dom_alg / dom_us / 1e3 / peaks["hbm_gbs"], 4)}},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": sum(M * K_DEC * 2 for M in SWEEP),
                 "d2h_bytes_per_step": sum(M * N_DEC * 2 for M in SWEEP),
@@ -760,7 +844,8 @@ def main():
                 "batched_copies_value": round(e2e_batched, 2),
                 "host_async_graph_value": round(e2e_async, 2),
                 "host_async_eager_value": round(e2e_eager, 2)},
-        "gpu_launches": args.steps * launches_per_step,
+        "host_us_per_call": host_us,
+        "gpu_launches": n_win * args.steps * n_launch,
         "clocks": clocks,
     }
     if not args.no_other_workloads:

@@ -81,8 +81,24 @@ enum skinny_gemm_status {
  * must not move while the handle lives (its contents may change between
  * runs).  Requirements: N >= 1, K >= 8, K % 8 == 0, W 16-byte aligned;
  * dtype SKG_BF16 or SKG_FP16; out_dtype SKG_FP32 or equal to dtype.
- * Allocates a small device status word (the watchdog).  Must not be called
- * while a stream on this device is capturing (returns NULL, ECAPTURING).
+ * Allocates a small device status word (the watchdog) and clears it with a
+ * synchronous memset, so it must be called before CUDA graph capture
+ * (low_latency_gemm page, autotune_kda_qkvg: compiled/tuned before capture).
+ * Refused with NULL / ECAPTURING, before any device work, when a capture is
+ * visible from the calling thread: the per-thread default stream capturing,
+ * or the legacy stream capturing or tied to a capturing blocking stream.  (A
+ * capture on a non-blocking stream in another thread is not visible; the
+ * allocation then fails with ECAPTURING and the driver may invalidate that
+ * capture.)
+ *
+ * Plan sources, by the environment variable SKINNY_GEMM_TUNE read here:
+ *   "off"    the built-in default tactic for every M (tactic file ignored);
+ *   "cache"  (default) the default plan, with the entries of the file named
+ *            by SKINNY_GEMM_TACTIC_FILE for this device/N/K/dtypes applied;
+ *   "full"   as "cache", then M = 1, 2, 4, 8, 16, 32, 48, 64 not found in the
+ *            file are autotuned here (skinny_gemm_autotune on the legacy
+ *            stream: synchronizes, allocates scratch) and appended to it.
+ * Any other value: NULL / EINVAL.  SKG_PREPARE_NO_TUNE_CACHE means "off".
  * Returns NULL on error (see skinny_gemm_last_error / skinny_gemm_last_status).
  */
 skinny_gemm_t skinny_gemm_prepare(const void* W, int64_t N, int64_t K, int dtype, int out_dtype);
@@ -161,6 +177,12 @@ int skinny_gemm_run_host_async(skinny_gemm_t h, const void* x_host, int64_t M, v
  * output and N_fb >= K_fb.  Records fork_event on main, makes aux wait on it,
  * records join_event on aux after the chain and makes main wait on it.  No
  * synchronization: the whole step can be captured from `main`.
+ * Every launch's arguments are checked before the fork is recorded: x, fa and
+ * out_fb must be 16-byte aligned device pointers (out_main too), and for
+ * chain > 1 the F_B rows must be 16-byte multiples (N_fb % 8 == 0), since each
+ * link reads the previous block by TMA.  A refused step enqueues nothing
+ * (EINVAL / EALIGN / EUNSUPPORTED_M); if a launch itself fails after the
+ * fork, the join is still recorded so aux is always joined back into main.
  */
 int skinny_gemm_run_overlap(skinny_gemm_t h_main, skinny_gemm_t h_fa, skinny_gemm_t h_fb,
                             int chain, const void* x, int64_t M, void* out_main, void* fa,
@@ -268,16 +290,20 @@ void skinny_gemm_destroy(skinny_gemm_t h);
  * Scratch: the kernels' one piece of scratch, the 4-byte watchdog status word,
  * lives in a static 256-byte device array inside the library (held on every
  * GPU that loads the library until the process exits).  A request needing more
- * scratch than 256 bytes is rejected with SKG_EINVAL and a message.  Each call
- * clears the word on `stream` before its launch; the word is not read back
- * (use the handle API for watchdog reports).  All calls share the array, so
- * calls that overlap on the GPU (different streams, or different host threads)
- * race on it; serialize them on one stream.
+ * scratch than 256 bytes is rejected with SKG_EINVAL and a message.  The array
+ * keeps the last call's contents; it is zeroed once, at set-up.  The word only
+ * goes from zero to a code (the first expired wait wins) and is not read back
+ * (use the handle API for watchdog reports), so no call needs it cleared and
+ * consecutive calls on one stream still overlap under programmatic dependent
+ * launch.  All calls share the array, so calls that overlap on the GPU
+ * (different streams, or different host threads) race on it; serialize them
+ * on one stream.
  *
  * Set-up: the first call on each device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current) and caches it; make that
- * first call before any stream capture.  Calls no cudaMalloc, cudaFree or
- * other allocating routine.  Asynchronous: returns after the launch.
+ * (cudaGetSymbolAddress, with that device current), zeroes the array with a
+ * synchronous cudaMemset and caches the address; make that first call before
+ * any stream capture.  Calls no cudaMalloc, cudaFree or other allocating
+ * routine.  Asynchronous: returns after the launch.
  * Errors: EINVAL, EALIGN, EUNSUPPORTED_M, EDEVICE, ECUDA.
  */
 int skinny_gemm_run_noalloc(const void* W, int64_t N, int64_t K, int64_t ldw, int out_dtype,

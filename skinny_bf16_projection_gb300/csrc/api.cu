@@ -51,6 +51,27 @@ int ok() {
   return SKG_OK;
 }
 
+// ECAPTURING when a capture that this call's allocations or synchronous copies
+// would disturb is visible from the calling thread: the per-thread default
+// stream capturing, or the legacy stream capturing or tied to a capturing
+// blocking stream (the legacy-stream query reports that without invalidating
+// the capture).  The per-thread stream is asked first, so a capture on it is
+// refused before the legacy stream is touched.  A capture on a non-blocking
+// stream is not visible here.
+int refuse_if_capturing(const char* what) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(cudaStreamPerThread, &cs);
+  if (e == cudaSuccess && cs == cudaStreamCaptureStatusNone)
+    e = cudaStreamIsCapturing(cudaStreamLegacy, &cs);
+  if (e == cudaErrorStreamCaptureImplicit ||
+      (e == cudaSuccess && cs != cudaStreamCaptureStatusNone)) {
+    (void)cudaGetLastError();
+    return fail(SKG_ECAPTURING, "%s must not be called while a stream is capturing", what);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+  return SKG_OK;
+}
+
 bool log_enabled() {
   static const bool on = [] {
     const char* v = getenv("SKINNY_GEMM_LOG");
@@ -98,6 +119,38 @@ int encode_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, in
     return fail(SKG_EINVAL, "cuTensorMapEncodeTiled failed (%d) for [%lld, %lld] pitch %lld box %d",
                 static_cast<int>(r), static_cast<long long>(rows), static_cast<long long>(cols),
                 static_cast<long long>(pitch), box_rows);
+  return SKG_OK;
+}
+
+// Tensor map of the activations x [M, K] (pitch ldx, box {64, tok}).  A decode
+// loop passes the same activation buffers call after call, so the encoded maps
+// are kept in a small per-thread cache keyed by everything the encoding reads
+// (a map holds no device state: reusing one for the same key is exact).
+struct XMapEntry {
+  const void* x = nullptr;
+  int64_t M = 0, K = 0, ldx = 0;
+  int tok = 0, dtype = -1;
+  CUtensorMap map{};
+};
+thread_local XMapEntry t_xmaps[16];
+
+int x_map(CUtensorMap* out, const void* x, int64_t M, int64_t K, int64_t ldx, int tok, int dtype) {
+  const uintptr_t key = reinterpret_cast<uintptr_t>(x) ^ static_cast<uintptr_t>(M * 0x9E3779B1ull) ^
+                        static_cast<uintptr_t>(tok << 3);
+  XMapEntry& e = t_xmaps[(key ^ (key >> 7) ^ (key >> 13)) & 15u];
+  if (e.x == x && e.M == M && e.K == K && e.ldx == ldx && e.tok == tok && e.dtype == dtype) {
+    *out = e.map;
+    return SKG_OK;
+  }
+  const int rc = encode_map(out, x, M, K, ldx, tok, dtype, CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
+  if (rc != SKG_OK) return rc;
+  e.x = x;
+  e.M = M;
+  e.K = K;
+  e.ldx = ldx;
+  e.tok = tok;
+  e.dtype = dtype;
+  e.map = *out;
   return SKG_OK;
 }
 
@@ -378,7 +431,7 @@ int launch_tactic(skinny_gemm_plan* h, const Tactic& t, const void* x, int64_t l
                   tactic_str(t).c_str());
   }
   CUtensorMap xmap;
-  int rc = encode_map(&xmap, x, M, h->K, ldx, t.tok, h->dtype, CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
+  int rc = x_map(&xmap, x, M, h->K, ldx, t.tok, h->dtype);
   if (rc != SKG_OK) return rc;
   KParams p{};
   p.out = out;
@@ -643,7 +696,22 @@ std::string cache_key(const skinny_gemm_plan* h) {
   return b;
 }
 
-void load_tactic_file(skinny_gemm_plan* h) {
+// SKINNY_GEMM_TUNE, read at prepare: "off" (the default plan only; the tactic
+// file is ignored), "cache" (the default: entries of SKINNY_GEMM_TACTIC_FILE
+// replace the default plan's), "full" (as "cache", then the decode token
+// counts the file has no entry for are autotuned at prepare and appended).
+// Returns 0, 1 or 2, or -1 for any other value.
+int tune_mode() {
+  const char* v = getenv("SKINNY_GEMM_TUNE");
+  if (v == nullptr || *v == '\0' || strcmp(v, "cache") == 0) return 1;
+  if (strcmp(v, "off") == 0) return 0;
+  if (strcmp(v, "full") == 0) return 2;
+  return -1;
+}
+
+// Applies the tactic file's entries for this weight to the plan and marks the
+// token counts it set in loaded[1..SKINNY_GEMM_MAX_M].
+void load_tactic_file(skinny_gemm_plan* h, bool* loaded) {
   const char* path = getenv("SKINNY_GEMM_TACTIC_FILE");
   if (path == nullptr || *path == '\0') return;
   FILE* f = fopen(path, "r");
@@ -658,7 +726,10 @@ void load_tactic_file(skinny_gemm_plan* h) {
     if (sscanf(line, "%599s %d %95s %lf", k, &m, ts, &us) < 3) continue;
     Tactic t;
     if (key != k || m < 1 || m > SKINNY_GEMM_MAX_M || !tactic_parse(ts, &t)) continue;
-    if (tactic_fits(h, t, m, nullptr) && active_clusters(h, t) > 0) h->plan[m] = t;  // last wins
+    if (tactic_fits(h, t, m, nullptr) && active_clusters(h, t) > 0) {  // last wins
+      h->plan[m] = t;
+      loaded[m] = true;
+    }
   }
   fclose(f);
 }
@@ -760,6 +831,11 @@ skinny_gemm_t skinny_gemm_prepare_ex(const void* W, int64_t N, int64_t K, int64_
            nullptr;
   if (reinterpret_cast<uintptr_t>(W) % 16 != 0)
     return fail(SKG_EALIGN, "weight base must be 16-byte aligned"), nullptr;
+  const int mode = (flags & SKG_PREPARE_NO_TUNE_CACHE) ? 0 : tune_mode();
+  if (mode < 0)
+    return fail(SKG_EINVAL, "SKINNY_GEMM_TUNE must be off, cache or full"), nullptr;
+  // prepare allocates and clears device memory, which a capture must not see
+  if (refuse_if_capturing("skinny_gemm_prepare") != SKG_OK) return nullptr;
 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -798,12 +874,17 @@ skinny_gemm_t skinny_gemm_prepare_ex(const void* W, int64_t N, int64_t K, int64_
   }
   for (int m = 1; m <= SKINNY_GEMM_MAX_M; ++m) h->plan[m] = default_tactic(h, m);
   h->pdl = !(flags & SKG_PREPARE_NO_PDL);
-  if (!(flags & SKG_PREPARE_NO_TUNE_CACHE)) load_tactic_file(h);
+  bool loaded[SKINNY_GEMM_MAX_M + 1] = {};
+  if (mode >= 1) load_tactic_file(h, loaded);
+  bool forced = false;
   if (const char* f = getenv("SKINNY_GEMM_FORCE_TACTIC")) {
     Tactic t;
     if (tactic_parse(f, &t))
       for (int m = 1; m <= SKINNY_GEMM_MAX_M; ++m)
-        if (tactic_fits(h, t, m, nullptr)) h->plan[m] = t;
+        if (tactic_fits(h, t, m, nullptr)) {
+          h->plan[m] = t;
+          forced = true;
+        }
   }
   for (int m = 1; m <= SKINNY_GEMM_MAX_M; ++m) {
     if (!h->plan[m].valid()) {
@@ -826,6 +907,19 @@ skinny_gemm_t skinny_gemm_prepare_ex(const void* W, int64_t N, int64_t K, int64_
     fprintf(stderr, "\n");
   }
   register_handle(h);
+  if (mode == 2 && !forced) {
+    std::vector<int64_t> want;
+    for (int m : {1, 2, 4, 8, 16, 32, 48, 64})
+      if (!loaded[m]) want.push_back(m);
+    if (!want.empty() &&
+        skinny_gemm_autotune(h, want.data(), static_cast<int>(want.size()), nullptr) != SKG_OK) {
+      const int code = g_last_status;
+      const std::string msg = g_err;
+      skinny_gemm_destroy(h);
+      fail(code, "SKINNY_GEMM_TUNE=full: %s", msg.c_str());
+      return nullptr;
+    }
+  }
   ok();
   return h;
 }
@@ -866,7 +960,10 @@ int skinny_gemm_run_residual(skinny_gemm_t h, const void* x, int64_t ldx, int64_
 
 int skinny_gemm_run(skinny_gemm_t h, const void* x, int64_t M, void* out, void* stream) {
   if (check_handle(h) != SKG_OK) return SKG_EINVAL;
-  return skinny_gemm_run_strided(h, x, h->K, M, out, h->N, stream);
+  int rc = validate_args(h, x, h->K, M, out, h->N);
+  if (rc != SKG_OK) return rc;
+  rc = launch_tactic(h, h->plan[M], x, h->K, M, out, h->N, static_cast<cudaStream_t>(stream));
+  return rc == SKG_OK ? ok() : rc;
 }
 
 namespace {
@@ -889,7 +986,7 @@ int enqueue_host(skinny_gemm_t h, const void* x_host, int64_t M, void* out_host,
   }
   e = cudaMemcpyAsync(h->x_stage, x_host, static_cast<size_t>(M) * h->K * 2, cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(x)");
-  int rc = skinny_gemm_run(h, h->x_stage, M, h->out_stage, st);
+  int rc = launch_tactic(h, h->plan[M], h->x_stage, h->K, M, h->out_stage, h->N, st);
   if (rc != SKG_OK) return rc;
   e = cudaMemcpyAsync(out_host, h->out_stage, static_cast<size_t>(M) * h->N * out_elem_bytes(h),
                       cudaMemcpyDeviceToHost, st);
@@ -928,10 +1025,22 @@ int overlap_impl(skinny_gemm_t h_main, skinny_gemm_t h_fa, skinny_gemm_t h_fb, i
     return fail(SKG_EINVAL, "a chain needs bf16 F_B output with N_fb >= K_fb");
   if (fork_event == nullptr || join_event == nullptr || aux_stream == nullptr)
     return fail(SKG_EINVAL, "overlap needs an aux stream and two events");
+  // Every launch's arguments are checked before the fork is recorded, so a
+  // refused step enqueues nothing (a capture stays consistent).
   int rc = validate_args(h_main, x, h_main->K, M, out_main, h_main->N);
   if (rc != SKG_OK) return rc;
   rc = validate_args(h_fa, x, h_fa->K, M, fa, h_fa->N);
   if (rc != SKG_OK) return rc;
+  rc = validate_args(h_fb, fa, h_fb->K, M, out_fb, h_fb->N);  // link 1 reads fa
+  if (rc != SKG_OK) return rc;
+  const size_t blk = static_cast<size_t>(M) * h_fb->N * out_elem_bytes(h_fb);
+  char* fb = static_cast<char*>(out_fb);
+  if (chain > 1) {
+    // link i > 1 reads the first K_fb columns of link i-1's block (pitch N_fb)
+    if (blk % 16 != 0) return fail(SKG_EALIGN, "out_fb blocks of a chain must be 16-byte multiples");
+    rc = validate_args(h_fb, fb, h_fb->N, M, fb + blk, h_fb->N);
+    if (rc != SKG_OK) return rc;
+  }
   cudaStream_t ms = static_cast<cudaStream_t>(main_stream);
   cudaStream_t as = static_cast<cudaStream_t>(aux_stream);
   cudaEvent_t fork = static_cast<cudaEvent_t>(fork_event);
@@ -942,21 +1051,18 @@ int overlap_impl(skinny_gemm_t h_main, skinny_gemm_t h_fa, skinny_gemm_t h_fb, i
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent(aux, fork)");
   // Aux chain first so its small grids are queued before the big one fills the GPU.
   rc = launch_tactic(h_fa, h_fa->plan[M], x, h_fa->K, M, fa, h_fa->N, as);
-  if (rc != SKG_OK) return rc;
-  const size_t blk = static_cast<size_t>(M) * h_fb->N * out_elem_bytes(h_fb);
-  char* fb = static_cast<char*>(out_fb);
-  rc = launch_tactic(h_fb, h_fb->plan[M], fa, h_fb->K, M, fb, h_fb->N, as);
-  if (rc != SKG_OK) return rc;
-  for (int i = 1; i < chain; ++i) {
+  if (rc == SKG_OK) rc = launch_tactic(h_fb, h_fb->plan[M], fa, h_fb->K, M, fb, h_fb->N, as);
+  for (int i = 1; i < chain && rc == SKG_OK; ++i)
     rc = launch_tactic(h_fb, h_fb->plan[M], fb + (i - 1) * blk, h_fb->N, M, fb + i * blk, h_fb->N, as);
-    if (rc != SKG_OK) return rc;
-  }
+  if (rc == SKG_OK) rc = launch_tactic(h_main, h_main->plan[M], x, h_main->K, M, out_main, h_main->N, ms);
+  // The join is recorded even after a failed launch, so the aux stream is
+  // always joined back into main (a capture would otherwise be left unjoined).
+  const std::string why = g_err;
+  const int code = rc;
   e = cudaEventRecord(join, as);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(join)");
-  rc = launch_tactic(h_main, h_main->plan[M], x, h_main->K, M, out_main, h_main->N, ms);
-  if (rc != SKG_OK) return rc;
-  e = cudaStreamWaitEvent(ms, join, 0);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent(main, join)");
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ms, join, 0);
+  if (code != SKG_OK) return fail(code, "%s", why.c_str());
+  if (e != cudaSuccess) return cuda_fail(e, "overlap join");
   return ok();
 }
 }  // namespace
@@ -1478,13 +1584,17 @@ uint32_t* g_noalloc_addr[64] = {};
 
 // Device address of the scratch array on device `dev` (which must be current).
 // Host code cannot pass `g_noalloc_scratch` itself to a kernel: on the host
-// that name is a stand-in, not a device address.  Looked up once per device.
+// that name is a stand-in, not a device address.  Looked up once per device;
+// the array is zeroed then, with a synchronous memset (set-up happens outside
+// any capture), so no later call has to clear it.
 int noalloc_scratch_address(int dev, uint32_t** out) {
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
   if (g_noalloc_addr[dev] == nullptr) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-alloc scratch)");
+    e = cudaMemset(p, 0, kNoAllocScratchBytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(no-alloc scratch)");
     g_noalloc_addr[dev] = static_cast<uint32_t*>(p);
   }
   *out = g_noalloc_addr[dev];
@@ -1536,9 +1646,11 @@ extern "C" int skinny_gemm_run_noalloc(const void* W, int64_t N, int64_t K, int6
   rc = encode_map(t.rows == 64 ? &p.wmap64 : &p.wmap128, W, N, K, ldw, t.rows, SKG_BF16,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   if (rc != SKG_OK) return rc;
-  // The array keeps the previous call's contents: the status word must start at zero.
-  e = cudaMemsetAsync(scratch, 0, need, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(no-alloc scratch)");
+  // The array keeps the previous call's contents.  The status word is the
+  // only part a kernel touches, it only ever goes from zero to a code (first
+  // expiry wins) and nothing reads it back, so no call needs it cleared; with
+  // no clearing node between them, consecutive calls on a stream still overlap
+  // under programmatic dependent launch.
   rc = launch_tactic(&p, t, x, ldx, M, out, ldo, static_cast<cudaStream_t>(stream));
   return rc == SKG_OK ? ok() : rc;
 }
