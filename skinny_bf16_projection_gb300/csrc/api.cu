@@ -688,12 +688,17 @@ Tactic default_tactic(const skinny_gemm_plan* h, int64_t M) {
 // ------------------------------------------------------------------ tactic file
 const char* out_name(int d) { return d == SKG_FP32 ? "fp32" : (d == SKG_FP16 ? "fp16" : "bf16"); }
 
+// One whitespace-free word (a tactic-file line is "<key> <M> <tactic> <us>"):
+// blanks in the device name ("NVIDIA GB300") become '_'.
 std::string cache_key(const skinny_gemm_plan* h) {
   char b[512];
   snprintf(b, sizeof b, "%s|sm%d|N%lld|K%lld|in%s|out%s|abi%d", h->dev->name, h->dev->sm_count,
            static_cast<long long>(h->N), static_cast<long long>(h->K), out_name(h->dtype),
            out_name(h->out_dtype), SKINNY_GEMM_ABI_VERSION);
-  return b;
+  std::string k = b;
+  for (char& c : k)
+    if (c == ' ' || c == '\t' || c == '\n' || c == '\r') c = '_';
+  return k;
 }
 
 // SKINNY_GEMM_TUNE, read at prepare: "off" (the default plan only; the tactic
@@ -732,6 +737,21 @@ void load_tactic_file(skinny_gemm_plan* h, bool* loaded) {
     }
   }
   fclose(f);
+}
+
+// Token counts without an entry of their own take the tactic of the smallest
+// M' > M that has one (known[M']), when it fits M: the rule skinny_gemm_autotune
+// applies to the token counts it did not time, so a plan rebuilt from the
+// tactic file matches the tuned one.
+void propagate_plan(skinny_gemm_plan* h, const bool* known) {
+  for (int m = 1; m <= SKINNY_GEMM_MAX_M; ++m) {
+    if (known[m]) continue;
+    for (int mp = m + 1; mp <= SKINNY_GEMM_MAX_M; ++mp)
+      if (known[mp]) {
+        if (tactic_fits(h, h->plan[mp], m, nullptr)) h->plan[m] = h->plan[mp];
+        break;
+      }
+  }
 }
 
 void append_tactic_file(const skinny_gemm_plan* h, int64_t M, const Tactic& t, double us) {
@@ -875,7 +895,10 @@ skinny_gemm_t skinny_gemm_prepare_ex(const void* W, int64_t N, int64_t K, int64_
   for (int m = 1; m <= SKINNY_GEMM_MAX_M; ++m) h->plan[m] = default_tactic(h, m);
   h->pdl = !(flags & SKG_PREPARE_NO_PDL);
   bool loaded[SKINNY_GEMM_MAX_M + 1] = {};
-  if (mode >= 1) load_tactic_file(h, loaded);
+  if (mode >= 1) {
+    load_tactic_file(h, loaded);
+    propagate_plan(h, loaded);
+  }
   bool forced = false;
   if (const char* f = getenv("SKINNY_GEMM_FORCE_TACTIC")) {
     Tactic t;
@@ -911,8 +934,24 @@ skinny_gemm_t skinny_gemm_prepare_ex(const void* W, int64_t N, int64_t K, int64_
     std::vector<int64_t> want;
     for (int m : {1, 2, 4, 8, 16, 32, 48, 64})
       if (!loaded[m]) want.push_back(m);
-    if (!want.empty() &&
-        skinny_gemm_autotune(h, want.data(), static_cast<int>(want.size()), nullptr) != SKG_OK) {
+    std::vector<Tactic> from_file(h->plan, h->plan + SKINNY_GEMM_MAX_M + 1);
+    int rc = SKG_OK;
+    if (!want.empty())
+      rc = skinny_gemm_autotune(h, want.data(), static_cast<int>(want.size()), nullptr);
+    if (rc == SKG_OK) {
+      // The tuner spreads its picks over the token counts it did not time; the
+      // file's entries stay, and the rest follow the nearest entry above.
+      bool known[SKINNY_GEMM_MAX_M + 1] = {};
+      for (int m = 1; m <= SKINNY_GEMM_MAX_M; ++m)
+        if (loaded[m]) {
+          h->plan[m] = from_file[m];
+          known[m] = true;
+        }
+      for (int64_t m : want) known[m] = true;
+      propagate_plan(h, known);
+      for (int m = 1; m <= SKINNY_GEMM_MAX_M && rc == SKG_OK; ++m) rc = ensure_workspace(h, h->plan[m]);
+    }
+    if (rc != SKG_OK) {
       const int code = g_last_status;
       const std::string msg = g_err;
       skinny_gemm_destroy(h);

@@ -231,14 +231,13 @@ __global__ void __launch_bounds__(160) skinny_mma_kernel(const __grid_constant__
     }
   }
   __syncthreads();
-  bool received = true;
-  if (csize > 1) {
-    received = mbar_wait_bounded<true>(recv_bar, 0, p.timeout_ns);
-    if (!received) report_status(p.status, kStatusTimeoutRecv);
-    // Arrive once every peer's pushes have landed here (or the wait gave up);
-    // the matching wait before exit keeps this CTA's shared memory alive until
-    // every peer has pushed, even on the timeout path.
-    cluster_arrive_release();
+  if (csize > 1 && !mbar_wait_bounded<true>(recv_bar, 0, p.timeout_ns)) {
+    report_status(p.status, kStatusTimeoutRecv);
+    // A live peer pushes after at most one bounded wait per pipeline stage of
+    // its K range (at most iters + 1 stages): keep waiting that many more
+    // rounds, so this CTA does not exit while a peer may still push into it.
+    for (int r = 0; r < iters + 2; ++r)
+      if (mbar_wait_bounded<true>(recv_bar, 0, p.timeout_ns)) break;
   }
   const int nbase = n0 + static_cast<int>(rank) * RS;
   for (int idx = threadIdx.x; idx < RS * M; idx += blockDim.x) {
@@ -256,13 +255,6 @@ __global__ void __launch_bounds__(160) skinny_mma_kernel(const __grid_constant__
       if (!mbar_wait_bounded(full_bar(s), static_cast<uint32_t>(last / S) & 1u, p.timeout_ns))
         report_status(p.status, kStatusTimeoutDrain);
     }
-  }
-  if (csize > 1) {
-    cluster_wait_acquire();
-    // After an expired receive wait, the peers' pushes were all issued before
-    // they arrived: wait (bounded) for them to land before the CTA exits.
-    if (!received && !mbar_wait_bounded<true>(recv_bar, 0, p.timeout_ns))
-      report_status(p.status, kStatusTimeoutDrain);
   }
 }
 

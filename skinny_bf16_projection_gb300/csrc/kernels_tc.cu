@@ -223,7 +223,6 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
     }
   };
 
-  bool received = true;  // st.async path: the receive wait completed
   if (csize == 1) {
     const int n = n0 + r;
     for (int c0 = 0; c0 < TOK && c0 < M; c0 += CH) {
@@ -333,12 +332,15 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
       }
     }
     __syncthreads();
-    received = mbar_wait_bounded<true>(recv_bar, 0, p.timeout_ns);
-    if (!received) report_status(p.status, kStatusTimeoutRecv);
-    // Arrive once every peer's pushes have landed here (or the wait gave up);
-    // the matching wait before exit keeps this CTA's shared memory alive until
-    // every peer has pushed, even on the timeout path.
-    cluster_arrive_release();
+    if (!mbar_wait_bounded<true>(recv_bar, 0, p.timeout_ns)) {
+      report_status(p.status, kStatusTimeoutRecv);
+      // A live peer pushes after at most one bounded wait per pipeline stage of
+      // its K range (at most iters + 1 stages) and one for its MMAs: keep
+      // waiting that many more rounds, so this CTA does not exit while a peer
+      // may still push into it.
+      for (int r = 0; r < iters + 3; ++r)
+        if (mbar_wait_bounded<true>(recv_bar, 0, p.timeout_ns)) break;
+    }
     // Reduce in rank order (deterministic) 8 rows x 1 token per step (lanes
     // walk the token index: conflict-free reads) and store the 8 outputs,
     // contiguous in out[t], with 16-byte stores where aligned.
@@ -378,13 +380,6 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
       if (!mbar_wait_bounded(full_bar(s), static_cast<uint32_t>(last / S) & 1u, p.timeout_ns))
         report_status(p.status, kStatusTimeoutDrain);
     }
-  }
-  if (csize > 1 && !bulk) {
-    cluster_wait_acquire();
-    // After an expired receive wait, the peers' pushes were all issued before
-    // they arrived: wait (bounded) for them to land before the CTA exits.
-    if (!received && !mbar_wait_bounded<true>(recv_bar, 0, p.timeout_ns))
-      report_status(p.status, kStatusTimeoutDrain);
   }
 }
 
