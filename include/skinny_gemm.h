@@ -67,6 +67,13 @@ enum skinny_gemm_status {
  * prologue no longer overlaps that kernel (for measuring what the overlap
  * hides, or for streams mixing kernels that must not overlap at all). */
 #define SKG_PREPARE_NO_PDL 0x2u
+/* Keep every output bit-reproducible run to run: the autotuners then leave
+ * out tactics with run-time K sharing (":w", see skinny_gemm_set_tactic),
+ * whose fp32 summation order depends on which CTA of a cluster took which
+ * K box.  Without this flag a tuned plan may use them (each result is still
+ * within the acceptance bound; only its last bits may vary).  The default,
+ * untuned plan always has a fixed order. */
+#define SKG_PREPARE_DETERMINISTIC 0x4u
 
 /*
  * Prepare a projection for weight W[N, K] (packed, row pitch K).
@@ -225,22 +232,29 @@ int skinny_gemm_autotune_overlap(skinny_gemm_t h_main, skinny_gemm_t h_fa, skinn
 
 /* Force the tactic used for token count M (1..256), given as the string
  * skinny_gemm_plan_query prints:
- *   "tc:r128:t<tok>:b<boxes>:s<stages>:c<cluster>[:d<k>][:a]"  tcgen05 kernel
- *   "mma:r<64|128>:t<tok>:b<boxes>:s<stages>:c<cluster>[:d<k>]"  mma.sync kernel
+ *   "tc:r<64|128>:t<tok>:b<boxes>:s<stages>:c<cluster>[:d<k>][:p<k>][:a][:w]"  tcgen05
+ *   "mma:r<64|128>:t<tok>:b<boxes>:s<stages>:c<cluster>[:d<k>][:p<k>][:w]"  mma.sync
  *   "sk:r128:t<tok>:b<boxes>:s<stages>:<g|p><n>"             stream-K kernel
  * (t = token tile, b = 64-wide K boxes per pipeline stage, c = split-K cluster
  * size, g = CTAs per SM / p = parts per row tile for stream-K; d<k> launches
  * the next kernel on the stream (PDL) only once all but k-1 of a CTA's weight
- * stages are issued; :a places a cluster's receive buffer in the pipeline
+ * stages are issued; p<k> (not with :w) also brings the weight boxes of the
+ * k stages after the first ones into L2 before the PDL wait, so they are
+ * fetched while the previous kernel finishes; :a places a cluster's receive
+ * buffer in the pipeline
  * stages, which frees shared memory for more CTAs per SM at the price of a
- * cluster barrier after the MMAs).  tcgen05 tactics with tok < M run
+ * cluster barrier after the MMAs; :w, with c > 1 and not with :a, shares a
+ * cluster's K boxes out at run time: after its first `s` stages, whose boxes
+ * are fixed, each CTA takes the next boxes from a counter in the cluster's
+ * first CTA, so the CTAs of a cluster end their K work together; the fp32
+ * summation order then varies from run to run).  tcgen05 tactics with tok < M run
  * ceil(M / tok) token tiles; the other kernels need tok >= M.  EINVAL if the string does not
  * parse or the tactic does not fit this weight and M. */
 int skinny_gemm_set_tactic(skinny_gemm_t h, int64_t M, const char* tactic);
 
 /* Parse a tactic string (grammar at skinny_gemm_set_tactic) and write its
  * canonical spelling into buf (NUL-terminated, truncated to len): suffixes in
- * the order ":d<k>", ":a".  No handle and no device needed.  EINVAL if it does
+ * the order ":d<k>", ":p<k>", ":a", ":w".  No handle and no device needed.  EINVAL if it does
  * not parse. */
 int skinny_gemm_tactic_normalize(const char* tactic, char* buf, size_t len);
 

@@ -46,10 +46,12 @@ class Projection:
     ``weight`` [N, K] (bf16 or fp16, CUDA, unit inner stride) is borrowed: this
     object keeps a reference so it stays alive, and it must not be moved or
     resized.  ``out_dtype`` is torch.float32 or the weight's own dtype (default).
+    ``deterministic=True`` keeps the autotuner to tactics with a fixed fp32
+    summation order (SKG_PREPARE_DETERMINISTIC).
     """
 
     def __init__(self, weight: torch.Tensor, out_dtype: torch.dtype | None = None, *,
-                 use_tactic_file: bool = True, pdl: bool = True):
+                 use_tactic_file: bool = True, pdl: bool = True, deterministic: bool = False):
         if out_dtype is None:
             out_dtype = weight.dtype
         if not weight.is_cuda:
@@ -63,7 +65,8 @@ class Projection:
         with torch.cuda.device(weight.device):
             h = self._lib.skinny_gemm_prepare_ex(
                 ptr, weight.shape[0], weight.shape[1], ldw, _IN_CODES[weight.dtype],
-                _OUT_CODES[out_dtype], (0 if use_tactic_file else 1) | (0 if pdl else 2))
+                _OUT_CODES[out_dtype],
+                (0 if use_tactic_file else 1) | (0 if pdl else 2) | (4 if deterministic else 0))
         if not h:
             raise SkinnyGemmError(self._lib.skinny_gemm_last_status(), _native.last_error())
         self._h = ctypes.c_void_p(h)

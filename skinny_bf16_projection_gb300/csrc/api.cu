@@ -161,20 +161,25 @@ struct Tactic {
   int variant = 0, rows = 0, tok = 0, nbox = 0, stages = 0, cl = 0, mode = 0;
   int lt = 0;  // k >= 1: launch dependents only with k-1 stages' loads left to issue (mma / tc)
   int al = 0;  // 1: tcgen05 cluster receive buffer aliases the pipeline stages
+  int dy = 0;  // 1: K boxes after the first stages shared out at run time within the cluster
+  int pf = 0;  // k >= 1: the next k stages' weight boxes prefetched into L2 before the PDL wait
   bool valid() const { return variant != 0; }
 };
 
 // "tc:r128:t16:b2:s4:c8" (c = cluster size) or "sk:r128:t16:b2:s5:g1" (g = CTAs per SM),
-// with ":d<k>" appended for a late PDL trigger (mma / tc) and ":a" for a tcgen05
-// cluster reduction buffer aliased onto the pipeline stages.
+// with ":d<k>" appended for a late PDL trigger (mma / tc), ":a" for a tcgen05
+// cluster reduction buffer aliased onto the pipeline stages, ":w" for K boxes
+// shared out at run time within a cluster and ":p<k>" for k stages of weight
+// boxes prefetched into L2 before the PDL wait.
 std::string tactic_str(const Tactic& t) {
   char b[96];
   const char* kind = t.variant == kVariantTc ? "tc" : (t.variant == kVariantSk ? "sk" : "mma");
   const char last = t.variant != kVariantSk ? 'c' : (t.mode == 1 ? 'p' : 'g');
-  char lt[16] = "";
+  char lt[16] = "", pf[16] = "";
   if (t.lt > 0) snprintf(lt, sizeof lt, ":d%d", t.lt);
-  snprintf(b, sizeof b, "%s:r%d:t%d:b%d:s%d:%c%d%s%s", kind, t.rows, t.tok, t.nbox, t.stages, last,
-           t.cl, lt, t.al ? ":a" : "");
+  if (t.pf > 0) snprintf(pf, sizeof pf, ":p%d", t.pf);
+  snprintf(b, sizeof b, "%s:r%d:t%d:b%d:s%d:%c%d%s%s%s%s", kind, t.rows, t.tok, t.nbox, t.stages,
+           last, t.cl, lt, pf, t.al ? ":a" : "", t.dy ? ":w" : "");
   return b;
 }
 
@@ -186,7 +191,7 @@ bool tactic_parse(const char* s, Tactic* t) {
   if (s == nullptr || sscanf(s, "%15[^:]:r%d:t%d:b%d:s%d:%c%d%n", kind, &x.rows, &x.tok, &x.nbox,
                              &x.stages, &last, &x.cl, &used) != 7)
     return false;
-  // optional suffixes, in any order, each at most once: ":d<k>", ":a"
+  // optional suffixes, in any order, each at most once: ":d<k>", ":p<k>", ":a", ":w"
   const char* rest = s + used;
   while (*rest != '\0') {
     if (strncmp(rest, ":d", 2) == 0 && x.lt == 0) {
@@ -194,8 +199,16 @@ bool tactic_parse(const char* s, Tactic* t) {
       if (sscanf(rest, ":d%d%n", &k, &n2) != 1 || k < 1 || k > 64) return false;
       x.lt = k;
       rest += n2;
+    } else if (strncmp(rest, ":p", 2) == 0 && x.pf == 0) {
+      int k = 0, n2 = 0;
+      if (sscanf(rest, ":p%d%n", &k, &n2) != 1 || k < 1 || k > 16) return false;
+      x.pf = k;
+      rest += n2;
     } else if (strncmp(rest, ":a", 2) == 0 && (rest[2] == '\0' || rest[2] == ':') && x.al == 0) {
       x.al = 1;
+      rest += 2;
+    } else if (strncmp(rest, ":w", 2) == 0 && (rest[2] == '\0' || rest[2] == ':') && x.dy == 0) {
+      x.dy = 1;
       rest += 2;
     } else {
       return false;
@@ -212,6 +225,8 @@ bool tactic_parse(const char* s, Tactic* t) {
     return false;
   if (x.lt && x.variant == kVariantSk) return false;
   if (x.al && x.variant != kVariantTc) return false;
+  if (x.dy && x.variant == kVariantSk) return false;
+  if (x.pf && (x.variant == kVariantSk || x.dy)) return false;
   *t = x;
   return true;
 }
@@ -319,6 +334,7 @@ struct skinny_gemm_plan {
   uint64_t timeout_ns = 2000000000ull;
   int debug_count = 0;
   bool pdl = true;  // programmatic dependent launch attribute on every launch
+  bool deterministic = false;  // the tuner keeps a fixed summation order (no :w tactics)
   uint64_t debug_timeout_ns = 0;
 };
 
@@ -331,8 +347,10 @@ int ntiles_of(const skinny_gemm_plan* h, const Tactic& t) {
 }
 uint32_t tactic_smem(const Tactic& t) {
   if (t.variant == kVariantSk) return sk_smem_bytes(t.tok, t.nbox, t.stages);
-  if (t.variant == kVariantTc) return tc_smem_bytes(t.tok, t.nbox, t.stages, t.cl, t.al != 0, t.rows);
-  return smem_bytes(t.rows, t.tok, t.nbox, t.stages);
+  const uint32_t dyn = t.dy ? kDynBytes : 0u;
+  if (t.variant == kVariantTc)
+    return tc_smem_bytes(t.tok, t.nbox, t.stages, t.cl, t.al != 0, t.rows) + dyn;
+  return smem_bytes(t.rows, t.tok, t.nbox, t.stages) + dyn;
 }
 // CTAs launched: row tiles x cluster size, or (stream-K) CTAs-per-SM x SMs,
 // capped at the number of work units.
@@ -383,6 +401,8 @@ bool tactic_fits(const skinny_gemm_plan* h, const Tactic& t, int64_t M, std::str
   if (t.al && (t.cl < 2 || static_cast<uint32_t>(t.stages) * stage_bytes(t.rows, t.tok, t.nbox) <
                                tc_red_bytes(t.tok, t.rows)))
     return no("an aliased receive buffer needs a cluster and stages at least as large");
+  if (t.dy && (t.cl < 2 || t.al))
+    return no("run-time K sharing (:w) needs a cluster and no aliased receive buffer");
   if (static_cast<int>(tactic_smem(t)) > h->dev->smem_optin)
     return no("shared memory footprint exceeds the per-block limit");
   return true;
@@ -448,6 +468,8 @@ int launch_tactic(skinny_gemm_plan* h, const Tactic& t, const void* x, int64_t l
   p.ldr = ldr;
   p.pdl_late = t.lt;
   p.red_alias = t.al;
+  p.dyn_k = t.dy;
+  p.l2_pre = t.pf;
   if (h->debug_count > 0) {
     --h->debug_count;
     p.debug_wait = 1;
@@ -894,6 +916,7 @@ skinny_gemm_t skinny_gemm_prepare_ex(const void* W, int64_t N, int64_t K, int64_
   }
   for (int m = 1; m <= SKINNY_GEMM_MAX_M; ++m) h->plan[m] = default_tactic(h, m);
   h->pdl = !(flags & SKG_PREPARE_NO_PDL);
+  h->deterministic = (flags & SKG_PREPARE_DETERMINISTIC) != 0;
   bool loaded[SKINNY_GEMM_MAX_M + 1] = {};
   if (mode >= 1) {
     load_tactic_file(h, loaded);
@@ -1498,19 +1521,56 @@ int skinny_gemm_autotune(skinny_gemm_t h, const int64_t* Ms, int nM, void* strea
       if (rc != SKG_OK) break;
       timed.push_back({us, t});
     }
-    // Phase 2: the fastest few again with later PDL triggers.
+    // Phase 2: the fastest few again with later PDL triggers; unless the handle
+    // is deterministic, the six fastest cluster tactics also with run-time K
+    // sharing (:w), and the best two of those with later triggers too.
     if (rc == SKG_OK) {
       std::stable_sort(timed.begin(), timed.end(),
                        [](const auto& a, const auto& b) { return a.first < b.first; });
-      const size_t top = std::min<size_t>(timed.size(), 3);
-      for (size_t c = 0; c < top && rc == SKG_OK; ++c) {
+      const std::vector<std::pair<double, Tactic>> base_timed = timed;
+      auto later_triggers = [&](const Tactic& t0) {
         for (int lt = 1; lt <= 4 && rc == SKG_OK; ++lt) {
-          Tactic t = timed[c].second;
+          Tactic t = t0;
           if (t.variant == kVariantSk || late_trigger_span(h, t) < lt) break;
           t.lt = lt;
           double us = 0;
           rc = time_tactic(t, &us);
           if (rc == SKG_OK) timed.push_back({us, t});
+        }
+      };
+      for (size_t c = 0; c < std::min<size_t>(base_timed.size(), 3) && rc == SKG_OK; ++c)
+        later_triggers(base_timed[c].second);
+      // The three fastest so far, each with 1, 2 or 4 stages prefetched into L2.
+      {
+        std::vector<std::pair<double, Tactic>> best3 = timed;
+        std::stable_sort(best3.begin(), best3.end(),
+                         [](const auto& a, const auto& b) { return a.first < b.first; });
+        for (size_t c = 0; c < std::min<size_t>(best3.size(), 3) && rc == SKG_OK; ++c)
+          for (int pf : {1, 2, 4}) {
+            Tactic t = best3[c].second;
+            if (t.variant == kVariantSk || late_trigger_span(h, t) < pf) break;
+            t.pf = pf;
+            double us = 0;
+            rc = time_tactic(t, &us);
+            if (rc == SKG_OK) timed.push_back({us, t});
+            if (rc != SKG_OK) break;
+          }
+      }
+      if (!h->deterministic) {
+        std::vector<std::pair<double, Tactic>> shared;
+        for (size_t c = 0; c < base_timed.size() && shared.size() < 6 && rc == SKG_OK; ++c) {
+          Tactic t = base_timed[c].second;
+          t.dy = 1;
+          if (!tactic_fits(h, t, M, nullptr) || active_clusters(h, t) <= 0) continue;
+          double us = 0;
+          rc = time_tactic(t, &us);
+          if (rc == SKG_OK) shared.push_back({us, t});
+        }
+        std::stable_sort(shared.begin(), shared.end(),
+                         [](const auto& a, const auto& b) { return a.first < b.first; });
+        for (size_t c = 0; c < shared.size(); ++c) {
+          timed.push_back(shared[c]);
+          if (c < 2 && rc == SKG_OK) later_triggers(shared[c].second);
         }
       }
     }

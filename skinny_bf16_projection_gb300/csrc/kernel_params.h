@@ -33,6 +33,10 @@ struct KParams {
   int32_t pdl_late;       // 0: launch dependents right after the first stages' weight loads;
                           // k >= 1: only once all but the last k-1 stages' loads are issued
   int32_t red_alias;      // tcgen05 clusters: the reduction buffer reuses the pipeline stages
+  int32_t dyn_k;          // clusters: K boxes after the first stages are shared out at run time
+                          // through a counter in the cluster's rank-0 CTA (see kDynBytes)
+  int32_t l2_pre;         // stages after the first ones whose weight boxes are prefetched
+                          // into L2 before the PDL wait (0: none)
   int32_t pad_;
   // stream-K kernel only: fp32 partial sums of split tiles and per-tile arrival counters
   float* workspace;       // [gridDim.x][2][TOK][128]
@@ -41,6 +45,11 @@ struct KParams {
   const void* residual;   // nullptr: none
   int64_t ldr;
 };
+
+// Run-time K sharing (dyn_k): a 16-byte slot holding the cluster's work counter
+// (used in rank 0) and one 32-bit box count per pipeline stage (at most 16),
+// placed after the barriers; added to the footprints below when dyn_k is set.
+constexpr uint32_t kDynBytes = 16 + 16 * 4;
 
 // Shared-memory footprint of one configuration (bytes, including 1 KB of
 // alignment slack).  Same formula on host and device.

@@ -71,6 +71,13 @@ __global__ void __launch_bounds__(160) skinny_mma_kernel(const __grid_constant__
   const int iters = (nb + NBOX - 1) / NBOX;
   const int RS = ROWS / static_cast<int>(csize);
   const int M = p.M;
+  // Run-time K sharing: the first stages hold fixed boxes (stage j of rank r:
+  // boxes starting at (j * csize + r) * NBOX), later ones whatever the
+  // cluster's counter hands out, so the CTAs of a cluster finish together.
+  const bool dyn = p.dyn_k != 0 && csize > 1;
+  const uint32_t dyn_area = bars + 8u * (2 * S + 4) + 16u;  // [counter | pad | counts[16]]
+  volatile uint32_t* const stage_boxes =
+      reinterpret_cast<volatile uint32_t*>(gbase + (dyn_area + 16u - base));
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -79,10 +86,15 @@ __global__ void __launch_bounds__(160) skinny_mma_kernel(const __grid_constant__
     }
     mbar_init(recv_bar, 1);
     if (csize > 1) mbar_arrive_expect_tx(recv_bar, (csize - 1) * RS * M * 4u);
+    if (dyn && rank == 0)  // boxes below S * csize * NBOX belong to the first stages
+      *reinterpret_cast<volatile uint32_t*>(gbase + (dyn_area - base)) =
+          static_cast<uint32_t>(S) * csize * NBOX;
     fence_mbar_init();
   }
   __syncthreads();
-  if (csize > 1) cluster_arrive_release();
+  if (csize > 1) cluster_arrive_release();  // counter and receive barrier initialised
+  bool start_waited = false;  // the producer waits for that before its first counter use
+  int n_armed = 0;            // producer: pipeline iterations armed (the drain below)
 
   float acc[MT][NT][4];
 #pragma unroll
@@ -93,63 +105,121 @@ __global__ void __launch_bounds__(160) skinny_mma_kernel(const __grid_constant__
       for (int c = 0; c < 4; ++c) acc[a][b][c] = 0.0f;
 
   if (warp == 0) {
+    // Producer state (lane 0's copy is the one used).
+    int pro = 0, trig = 0;
+    bool triggered = false;
+    uint64_t policy = 0;
     if (lane == 0) {
       prefetch_tensormap(&wmap);
       prefetch_tensormap(&xmap);
-      const uint64_t policy = l2_policy_evict_first();
-      const int pro = iters < S ? iters : S;
-      for (int it = 0; it < pro; ++it) {
-        const int nbi = min(NBOX, nb - it * NBOX);
-        const uint32_t st = base + static_cast<uint32_t>(it) * kStage;
-        mbar_arrive_expect_tx(full_bar(it), nbi * (kWBox + kXBox));
+      policy = l2_policy_evict_first();
+      // First box and box count of pipeline iteration `it` (fixed assignment;
+      // with dyn only the first S iterations, the prologue, are fixed).
+      auto fixed_box = [&](int it) {
+        return dyn ? (it * static_cast<int>(csize) + static_cast<int>(rank)) * NBOX : kb0 + it * NBOX;
+      };
+      auto fixed_count = [&](int it, int b0) {
+        return dyn ? max(0, min(NBOX, p.kboxes - b0)) : min(NBOX, nb - it * NBOX);
+      };
+      for (; pro < S && (dyn || pro < iters); ++pro) {
+        const int b0 = fixed_box(pro);
+        const int nbi = fixed_count(pro, b0);
+        if (nbi <= 0) break;
+        if (dyn) stage_boxes[pro] = static_cast<uint32_t>(nbi);
+        const uint32_t st = base + static_cast<uint32_t>(pro) * kStage;
+        mbar_arrive_expect_tx(full_bar(pro), nbi * (kWBox + kXBox));
         for (int b = 0; b < nbi; ++b)
-          tma_load_2d_hint(st + b * kWBox, &wmap, (kb0 + it * NBOX + b) * kBoxK, n0, full_bar(it),
-                           policy);
+          tma_load_2d_hint(st + b * kWBox, &wmap, (b0 + b) * kBoxK, n0, full_bar(pro), policy);
       }
+      // The weight boxes of the next l2_pre stages go to L2 now: these requests
+      // queue behind the previous grid's last loads and are served while it
+      // finishes, and the refills after the wait then read them from L2.
+      if (!dyn)
+        for (int it = pro; it < iters && it < pro + p.l2_pre; ++it)
+          for (int b = 0; b < min(NBOX, nb - it * NBOX); ++b)
+            tma_prefetch_2d(&wmap, (kb0 + it * NBOX + b) * kBoxK, n0);
       // Let the next kernel on the stream launch: its CTAs prefetch their own
       // weight tiles into whatever shared memory is free (they still wait for
       // our completion in griddepcontrol.wait before touching x or out).  By
       // default that happens now; with pdl_late it waits until this CTA has
       // issued (nearly) all of its weight loads, so the next grid's first
-      // loads queue up behind ours instead of competing with them.
-      const int trig = p.pdl_late > 0 ? max(pro, iters - p.pdl_late + 1) : pro;
-      if (trig == pro) pdl_launch_dependents();
+      // loads queue up behind ours instead of competing with them (with dyn
+      // the iteration count is estimated by the fixed split's).
+      trig = p.pdl_late > 0 ? max(pro, iters - p.pdl_late + 1) : pro;
+      triggered = trig == pro;
+      if (triggered) pdl_launch_dependents();
       pdl_wait();
       for (int it = 0; it < pro; ++it) {
-        const int nbi = min(NBOX, nb - it * NBOX);
+        const int b0 = fixed_box(it);
+        const int nbi = fixed_count(it, b0);
         const uint32_t st = base + static_cast<uint32_t>(it) * kStage + NBOX * kWBox;
         for (int b = 0; b < nbi; ++b)
-          tma_load_2d(st + b * kXBox, &xmap, (kb0 + it * NBOX + b) * kBoxK, 0, full_bar(it));
+          tma_load_2d(st + b * kXBox, &xmap, (b0 + b) * kBoxK, 0, full_bar(it));
       }
-      for (int it = pro; it < iters; ++it) {
-        if (it == trig) pdl_launch_dependents();
+    }
+    __syncwarp();
+    if (dyn) {
+      // The whole warp, converged (the cluster barrier is only ever used by
+      // complete warps): rank 0's counter is initialised.
+      cluster_wait_acquire();
+      start_waited = true;
+    }
+    if (lane == 0) {
+      const uint32_t counter = dyn ? mapa_shared(dyn_area, 0) : 0u;
+      // (dyn) the next chunk is taken from the counter as soon as the previous
+      // one's loads are issued, so the remote atomic's round trip overlaps the
+      // wait for a free stage instead of delaying the refill
+      int next_b0 = dyn ? static_cast<int>(atom_add_cluster_u32(counter, NBOX)) : 0;
+      int it = pro;
+      for (;; ++it) {
+        if (!dyn && it >= iters) break;
+        if (it == trig && !triggered) {
+          pdl_launch_dependents();
+          triggered = true;
+        }
         const int s = it % S;
-        const uint32_t ph = static_cast<uint32_t>((it / S) - 1) & 1u;
-        if (!mbar_wait_bounded(empty_bar(s), ph, p.timeout_ns))
-          report_status(p.status, kStatusTimeoutEmpty);
-        const int nbi = min(NBOX, nb - it * NBOX);
+        if (it >= S) {
+          const uint32_t ph = static_cast<uint32_t>((it / S) - 1) & 1u;
+          if (!mbar_wait_bounded(empty_bar(s), ph, p.timeout_ns))
+            report_status(p.status, kStatusTimeoutEmpty);
+        }
+        const int b0 = dyn ? next_b0 : kb0 + it * NBOX;
+        const int nbi = dyn ? max(0, min(NBOX, p.kboxes - b0)) : min(NBOX, nb - it * NBOX);
+        if (nbi <= 0) {  // (dyn) the cluster's boxes are all handed out: tell the consumers
+          stage_boxes[s] = 0u;
+          mbar_arrive(full_bar(s));
+          ++it;
+          break;
+        }
+        if (dyn) stage_boxes[s] = static_cast<uint32_t>(nbi);
         const uint32_t st = base + static_cast<uint32_t>(s) * kStage;
         mbar_arrive_expect_tx(full_bar(s), nbi * (kWBox + kXBox));
         for (int b = 0; b < nbi; ++b)
-          tma_load_2d_hint(st + b * kWBox, &wmap, (kb0 + it * NBOX + b) * kBoxK, n0, full_bar(s),
-                           policy);
+          tma_load_2d_hint(st + b * kWBox, &wmap, (b0 + b) * kBoxK, n0, full_bar(s), policy);
         for (int b = 0; b < nbi; ++b)
-          tma_load_2d(st + NBOX * kWBox + b * kXBox, &xmap, (kb0 + it * NBOX + b) * kBoxK, 0,
-                      full_bar(s));
+          tma_load_2d(st + NBOX * kWBox + b * kXBox, &xmap, (b0 + b) * kBoxK, 0, full_bar(s));
+        if (dyn) next_b0 = static_cast<int>(atom_add_cluster_u32(counter, NBOX));
       }
-      if (trig == iters && trig != pro) pdl_launch_dependents();
+      n_armed = it;
+      if (!triggered) pdl_launch_dependents();
     }
     __syncwarp();
   } else {
     pdl_wait();
     const int cw = static_cast<int>(warp) - 1;
     const int row_base = cw * MT * 16;
-    for (int it = 0; it < iters; ++it) {
+    // (dyn: a CTA consumes at most every box of the K range, plus the end marker)
+    const int max_it = dyn ? (p.kboxes + NBOX - 1) / NBOX + 1 : iters;
+    for (int it = 0; it < max_it; ++it) {
       const int s = it % S;
       const uint32_t ph = static_cast<uint32_t>(it / S) & 1u;
-      if (!mbar_wait_bounded(full_bar(s), ph, p.timeout_ns))
+      // (one decision per warp, so the warp stays converged for the cluster barrier)
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(full_bar(s), ph, p.timeout_ns))) {
         report_status(p.status, kStatusTimeoutFull);
-      const int nbi = min(NBOX, nb - it * NBOX);
+        if (dyn) break;  // the stage's box count cannot be trusted
+      }
+      const int nbi = dyn ? static_cast<int>(stage_boxes[s]) : min(NBOX, nb - it * NBOX);
+      if (nbi <= 0) break;
       const uint32_t wst = base + static_cast<uint32_t>(s) * kStage;
       const uint32_t xst = wst + NBOX * kWBox;
       for (int b = 0; b < nbi; ++b) {
@@ -195,7 +265,7 @@ __global__ void __launch_bounds__(160) skinny_mma_kernel(const __grid_constant__
 
   // ------------------------------------------------------------ epilogue
   pdl_wait();  // every thread that reads residual / writes out is ordered after the previous grid
-  if (csize > 1) cluster_wait_acquire();
+  if (csize > 1 && !start_waited) cluster_wait_acquire();
   if (warp > 0) {
     // Accumulator fragment: c0,c1 -> row g, tokens 2q, 2q+1; c2,c3 -> row g+8.
     const int cw = static_cast<int>(warp) - 1;
@@ -234,9 +304,11 @@ __global__ void __launch_bounds__(160) skinny_mma_kernel(const __grid_constant__
   if (csize > 1 && !mbar_wait_bounded<true>(recv_bar, 0, p.timeout_ns)) {
     report_status(p.status, kStatusTimeoutRecv);
     // A live peer pushes after at most one bounded wait per pipeline stage of
-    // its K range (at most iters + 1 stages): keep waiting that many more
-    // rounds, so this CTA does not exit while a peer may still push into it.
-    for (int r = 0; r < iters + 2; ++r)
+    // its K range (at most iters + 1 stages; with dyn, every box of K): keep
+    // waiting that many more rounds, so this CTA does not exit while a peer may
+    // still push into it.
+    const int rounds = (dyn ? (p.kboxes + NBOX - 1) / NBOX : iters) + 2;
+    for (int r = 0; r < rounds; ++r)
       if (mbar_wait_bounded<true>(recv_bar, 0, p.timeout_ns)) break;
   }
   const int nbase = n0 + static_cast<int>(rank) * RS;
@@ -248,10 +320,10 @@ __global__ void __launch_bounds__(160) skinny_mma_kernel(const __grid_constant__
     const int n = nbase + rs2;
     if (n < p.N) store_out<OutT>(p, t, n, sum);
   }
-  if (threadIdx.x == 0) {
-    const int used = iters < S ? iters : S;
+  if (threadIdx.x == 0) {  // the producer thread: every armed stage's last phase has landed
+    const int used = n_armed < S ? n_armed : S;
     for (int s = 0; s < used; ++s) {
-      const int last = s + ((iters - 1 - s) / S) * S;
+      const int last = s + ((n_armed - 1 - s) / S) * S;
       if (!mbar_wait_bounded(full_bar(s), static_cast<uint32_t>(last / S) & 1u, p.timeout_ns))
         report_status(p.status, kStatusTimeoutDrain);
     }

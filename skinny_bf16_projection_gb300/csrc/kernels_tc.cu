@@ -98,6 +98,16 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
   // Receive buffer: after the stages, or (aliased) at their start, or right
   // after the bulk path's staging area.
   const uint32_t red = !alias ? stages_end : (bulk ? base + kStageRed : base);
+  // Run-time K sharing (not with the aliased receive buffer): the first stages
+  // hold fixed boxes (stage j of rank r: boxes from (j * csize + r) * NBOX),
+  // later ones whatever the cluster's counter in rank 0 hands out, so the CTAs
+  // of a cluster finish their K work together.
+  const bool dyn = p.dyn_k != 0 && csize > 1 && !alias;
+  const uint32_t dyn_area = bars + 8u * (2 * S + 4) + 16u;  // [counter | pad | counts[16]]
+  volatile uint32_t* const stage_boxes =
+      reinterpret_cast<volatile uint32_t*>(gbase + (dyn_area + 16u - base));
+  // (dyn: a CTA whose first fixed box lies beyond K gets no box at all)
+  const bool has_work = dyn ? static_cast<int>(rank) * NBOX < p.kboxes : iters > 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -109,6 +119,9 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
     if (csize > 1)
       mbar_arrive_expect_tx(recv_bar, bulk ? (csize - 1) * static_cast<uint32_t>(M * RS) * 4u
                                            : (csize - 1) * RS * ((M + 3) / 4) * 16u);
+    if (dyn && rank == 0)  // boxes below S * csize * NBOX belong to the first stages
+      *reinterpret_cast<volatile uint32_t*>(gbase + (dyn_area - base)) =
+          static_cast<uint32_t>(S) * csize * NBOX;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -121,67 +134,127 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
   const uint32_t tmem = *tmem_slot_g;
   // matched by the wait before the pushes (aliased: arrive once the MMAs are done)
   if (csize > 1 && !alias) cluster_arrive_release();
+  bool start_waited = false;  // the producer waits for it before its first counter use
+  int n_armed = 0;            // producer: pipeline iterations armed (the drain below)
 
   if (warp == 0) {
+    // Producer state (lane 0's copy is the one used).
+    int pro = 0, trig = 0;
+    bool triggered = false;
+    uint64_t policy = 0;
     if (lane == 0) {
       prefetch_tensormap(&wmap);
       prefetch_tensormap(&xmap);
       // Weight tiles are streamed once (evict first), unless other token tiles'
       // CTAs read the same tiles again (then keep them at normal priority).
-      const uint64_t policy = gridDim.y > 1 ? l2_policy_evict_normal() : l2_policy_evict_first();
-      const int pro = iters < S ? iters : S;
-      for (int it = 0; it < pro; ++it) {
-        const int nbi = min(NBOX, nb - it * NBOX);
-        const uint32_t st = base + static_cast<uint32_t>(it) * kStage;
-        mbar_arrive_expect_tx(full_bar(it), nbi * (kWBox + kXBox));
+      policy = gridDim.y > 1 ? l2_policy_evict_normal() : l2_policy_evict_first();
+      // First box and box count of pipeline iteration `it` (fixed assignment;
+      // with dyn only the first S iterations, the prologue, are fixed).
+      auto fixed_box = [&](int it) {
+        return dyn ? (it * static_cast<int>(csize) + static_cast<int>(rank)) * NBOX : kb0 + it * NBOX;
+      };
+      auto fixed_count = [&](int it, int b0) {
+        return dyn ? max(0, min(NBOX, p.kboxes - b0)) : min(NBOX, nb - it * NBOX);
+      };
+      for (; pro < S && (dyn || pro < iters); ++pro) {
+        const int b0 = fixed_box(pro);
+        const int nbi = fixed_count(pro, b0);
+        if (nbi <= 0) break;
+        if (dyn) stage_boxes[pro] = static_cast<uint32_t>(nbi);
+        const uint32_t st = base + static_cast<uint32_t>(pro) * kStage;
+        mbar_arrive_expect_tx(full_bar(pro), nbi * (kWBox + kXBox));
         for (int b = 0; b < nbi; ++b)
-          tma_load_2d_hint(st + b * kWBox, &wmap, (kb0 + it * NBOX + b) * kBoxK, n0, full_bar(it),
-                           policy);
+          tma_load_2d_hint(st + b * kWBox, &wmap, (b0 + b) * kBoxK, n0, full_bar(pro), policy);
       }
+      // The weight boxes of the next l2_pre stages go to L2 now: these requests
+      // queue behind the previous grid's last loads and are served while it
+      // finishes, and the refills after the wait then read them from L2.
+      if (!dyn)
+        for (int it = pro; it < iters && it < pro + p.l2_pre; ++it)
+          for (int b = 0; b < min(NBOX, nb - it * NBOX); ++b)
+            tma_prefetch_2d(&wmap, (kb0 + it * NBOX + b) * kBoxK, n0);
       // Let the next kernel on the stream launch: its CTAs prefetch their own
       // weight tiles into whatever shared memory is free (they still wait for
       // our completion in griddepcontrol.wait before touching x or out).  By
       // default that happens now; with pdl_late it waits until this CTA has
       // issued (nearly) all of its weight loads, so the next grid's first
-      // loads queue up behind ours instead of competing with them.
-      const int trig = p.pdl_late > 0 ? max(pro, iters - p.pdl_late + 1) : pro;
-      if (trig == pro) pdl_launch_dependents();
+      // loads queue up behind ours instead of competing with them (with dyn
+      // the iteration count is estimated by the fixed split's).
+      trig = p.pdl_late > 0 ? max(pro, iters - p.pdl_late + 1) : pro;
+      triggered = trig == pro;
+      if (triggered) pdl_launch_dependents();
       pdl_wait();  // x is produced by the previous kernel on the stream
       for (int it = 0; it < pro; ++it) {
-        const int nbi = min(NBOX, nb - it * NBOX);
+        const int b0 = fixed_box(it);
+        const int nbi = fixed_count(it, b0);
         const uint32_t st = base + static_cast<uint32_t>(it) * kStage + NBOX * kWBox;
         for (int b = 0; b < nbi; ++b)
-          tma_load_2d(st + b * kXBox, &xmap, (kb0 + it * NBOX + b) * kBoxK, m0, full_bar(it));
+          tma_load_2d(st + b * kXBox, &xmap, (b0 + b) * kBoxK, m0, full_bar(it));
       }
-      for (int it = pro; it < iters; ++it) {
-        if (it == trig) pdl_launch_dependents();
+    }
+    __syncwarp();
+    if (dyn) {
+      // The whole warp, converged (the cluster barrier is only ever used by
+      // complete warps): rank 0's counter is initialised.
+      cluster_wait_acquire();
+      start_waited = true;
+    }
+    if (lane == 0) {
+      const uint32_t counter = dyn ? mapa_shared(dyn_area, 0) : 0u;
+      // (dyn) the next chunk is taken from the counter as soon as the previous
+      // one's loads are issued, so the remote atomic's round trip overlaps the
+      // wait for a free stage instead of delaying the refill
+      int next_b0 = dyn ? static_cast<int>(atom_add_cluster_u32(counter, NBOX)) : 0;
+      int it = pro;
+      for (;; ++it) {
+        if (!dyn && it >= iters) break;
+        if (it == trig && !triggered) {
+          pdl_launch_dependents();
+          triggered = true;
+        }
         const int s = it % S;
-        const uint32_t ph = static_cast<uint32_t>((it / S) - 1) & 1u;
-        if (!mbar_wait_bounded(empty_bar(s), ph, p.timeout_ns))
-          report_status(p.status, kStatusTimeoutEmpty);
-        const int nbi = min(NBOX, nb - it * NBOX);
+        if (it >= S) {
+          const uint32_t ph = static_cast<uint32_t>((it / S) - 1) & 1u;
+          if (!mbar_wait_bounded(empty_bar(s), ph, p.timeout_ns))
+            report_status(p.status, kStatusTimeoutEmpty);
+        }
+        const int b0 = dyn ? next_b0 : kb0 + it * NBOX;
+        const int nbi = dyn ? max(0, min(NBOX, p.kboxes - b0)) : min(NBOX, nb - it * NBOX);
+        if (nbi <= 0) {  // (dyn) the cluster's boxes are all handed out: tell the MMA issuer
+          stage_boxes[s] = 0u;
+          mbar_arrive(full_bar(s));
+          ++it;
+          break;
+        }
+        if (dyn) stage_boxes[s] = static_cast<uint32_t>(nbi);
         const uint32_t st = base + static_cast<uint32_t>(s) * kStage;
         mbar_arrive_expect_tx(full_bar(s), nbi * (kWBox + kXBox));
         for (int b = 0; b < nbi; ++b)
-          tma_load_2d_hint(st + b * kWBox, &wmap, (kb0 + it * NBOX + b) * kBoxK, n0, full_bar(s),
-                           policy);
+          tma_load_2d_hint(st + b * kWBox, &wmap, (b0 + b) * kBoxK, n0, full_bar(s), policy);
         for (int b = 0; b < nbi; ++b)
-          tma_load_2d(st + NBOX * kWBox + b * kXBox, &xmap, (kb0 + it * NBOX + b) * kBoxK, m0,
-                      full_bar(s));
+          tma_load_2d(st + NBOX * kWBox + b * kXBox, &xmap, (b0 + b) * kBoxK, m0, full_bar(s));
+        if (dyn) next_b0 = static_cast<int>(atom_add_cluster_u32(counter, NBOX));
       }
-      if (trig == iters && trig != pro) pdl_launch_dependents();
+      n_armed = it;
+      if (!triggered) pdl_launch_dependents();
     }
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
       pdl_wait();
-      for (int it = 0; it < iters; ++it) {
+      // (dyn: at most every box of the K range, plus the end marker)
+      const int max_it = dyn ? (p.kboxes + NBOX - 1) / NBOX + 1 : iters;
+      bool first = true;
+      for (int it = 0; it < max_it; ++it) {
         const int s = it % S;
         const uint32_t ph = static_cast<uint32_t>(it / S) & 1u;
-        if (!mbar_wait_bounded(full_bar(s), ph, p.timeout_ns))
+        if (!mbar_wait_bounded(full_bar(s), ph, p.timeout_ns)) {
           report_status(p.status, kStatusTimeoutFull);
+          if (dyn) break;  // the stage's box count cannot be trusted
+        }
         tc_fence_after_sync();
-        const int nbi = min(NBOX, nb - it * NBOX);
+        const int nbi = dyn ? static_cast<int>(stage_boxes[s]) : min(NBOX, nb - it * NBOX);
+        if (nbi <= 0) break;
         const uint32_t wst = base + static_cast<uint32_t>(s) * kStage;
         const uint32_t xst = wst + NBOX * kWBox;
         for (int b = 0; b < nbi; ++b) {
@@ -189,12 +262,18 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
           for (int j = 0; j < kBoxK / 16; ++j) {
             const uint64_t ad = sw128_kmajor_desc(wst + b * kWBox + j * 32);
             const uint64_t bd = sw128_kmajor_desc(xst + b * kXBox + j * 32);
-            tc_mma_f16kind(tmem, ad, bd, kIdesc, (it | b | j) != 0 ? 1u : 0u);
+            tc_mma_f16kind(tmem, ad, bd, kIdesc, first ? 0u : 1u);
+            first = false;
           }
         }
         tc_commit(empty_bar(s));
       }
-      tc_commit(done_bar);
+      // A CTA that got no K box (possible with run-time sharing) issued no MMA:
+      // arrive directly rather than through a commit with nothing to track.
+      if (first)
+        mbar_arrive(done_bar);
+      else
+        tc_commit(done_bar);
     }
     __syncwarp();
   }
@@ -219,7 +298,7 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
       float t16[16];
       tmem_ld_32x32b_x16(row_taddr + static_cast<uint32_t>(c0 + c * 16), t16);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) v[c * 16 + i] = iters > 0 ? t16[i] : 0.0f;
+      for (int i = 0; i < 16; ++i) v[c * 16 + i] = has_work ? t16[i] : 0.0f;
     }
   };
 
@@ -235,7 +314,7 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
       }
     }
   } else if (bulk) {
-    cluster_wait_acquire();  // every peer's receive barrier is initialised
+    if (!start_waited) cluster_wait_acquire();  // every peer's receive barrier is initialised
     // Token-major blocks [owner][TOK][RS]: each row's partial sums go to the
     // block of the CTA that owns the row, staged in this CTA's idle pipeline
     // buffers (every TMA load has landed and every MMA has read its operands
@@ -305,7 +384,7 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
     }
     cluster_wait_acquire();
   } else {
-    cluster_wait_acquire();  // every peer's receive barrier is initialised
+    if (!start_waited) cluster_wait_acquire();  // every peer's receive barrier is initialised
     // Receive buffer [rank][RS][TP]: each row's tokens contiguous (16-byte pushes),
     // rows padded by 4 floats so the reduce's 16-byte reads do not collide.
     constexpr int TP = TOK + 4;
@@ -338,7 +417,8 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
       // its K range (at most iters + 1 stages) and one for its MMAs: keep
       // waiting that many more rounds, so this CTA does not exit while a peer
       // may still push into it.
-      for (int r = 0; r < iters + 3; ++r)
+      const int rounds = (dyn ? (p.kboxes + NBOX - 1) / NBOX : iters) + 3;
+      for (int r = 0; r < rounds; ++r)
         if (mbar_wait_bounded<true>(recv_bar, 0, p.timeout_ns)) break;
     }
     // Reduce in rank order (deterministic) 8 rows x 1 token per step (lanes
@@ -372,11 +452,12 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
   if (threadIdx.x == 0) {
-    // Drain: every armed stage's last phase must have landed before exit
-    // (immediate on the normal path, where the MMA issuer waited for them).
-    const int used = iters < S ? iters : S;
+    // Drain (the producer thread): every armed stage's last phase must have
+    // landed before exit (immediate on the normal path, where the MMA issuer
+    // waited for them).
+    const int used = n_armed < S ? n_armed : S;
     for (int s = 0; s < used; ++s) {
-      const int last = s + ((iters - 1 - s) / S) * S;
+      const int last = s + ((n_armed - 1 - s) / S) * S;
       if (!mbar_wait_bounded(full_bar(s), static_cast<uint32_t>(last / S) & 1u, p.timeout_ns))
         report_status(p.status, kStatusTimeoutDrain);
     }
