@@ -232,7 +232,7 @@ int skinny_gemm_autotune_overlap(skinny_gemm_t h_main, skinny_gemm_t h_fa, skinn
 
 /* Force the tactic used for token count M (1..256), given as the string
  * skinny_gemm_plan_query prints:
- *   "tc:r<64|128>:t<tok>:b<boxes>:s<stages>:c<cluster>[:d<k>][:p<k>][:a][:w]"  tcgen05
+ *   "tc:r<64|128>:t<tok>:b<boxes>:s<stages>:c<cluster>[:d<k>][:p<k>][:a][:s][:w]"  tcgen05
  *   "mma:r<64|128>:t<tok>:b<boxes>:s<stages>:c<cluster>[:d<k>][:p<k>][:w]"  mma.sync
  *   "sk:r128:t<tok>:b<boxes>:s<stages>:<g|p><n>"             stream-K kernel
  * (t = token tile, b = 64-wide K boxes per pipeline stage, c = split-K cluster
@@ -243,7 +243,8 @@ int skinny_gemm_autotune_overlap(skinny_gemm_t h_main, skinny_gemm_t h_fa, skinn
  * fetched while the previous kernel finishes; :a places a cluster's receive
  * buffer in the pipeline
  * stages, which frees shared memory for more CTAs per SM at the price of a
- * cluster barrier after the MMAs; :w, with c > 1 and not with :a, shares a
+ * cluster barrier after the MMAs; :s (tcgen05 clusters at >= 64 tokens) sends the
+ * partial sums with per-thread stores instead of one bulk copy per peer; :w, with c > 1 and not with :a, shares a
  * cluster's K boxes out at run time: after its first `s` stages, whose boxes
  * are fixed, each CTA takes the next boxes from a counter in the cluster's
  * first CTA, so the CTAs of a cluster end their K work together; the fp32
@@ -254,7 +255,7 @@ int skinny_gemm_set_tactic(skinny_gemm_t h, int64_t M, const char* tactic);
 
 /* Parse a tactic string (grammar at skinny_gemm_set_tactic) and write its
  * canonical spelling into buf (NUL-terminated, truncated to len): suffixes in
- * the order ":d<k>", ":p<k>", ":a", ":w".  No handle and no device needed.  EINVAL if it does
+ * the order ":d<k>", ":p<k>", ":a", ":s", ":w".  No handle and no device needed.  EINVAL if it does
  * not parse. */
 int skinny_gemm_tactic_normalize(const char* tactic, char* buf, size_t len);
 

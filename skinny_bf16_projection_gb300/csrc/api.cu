@@ -163,6 +163,7 @@ struct Tactic {
   int al = 0;  // 1: tcgen05 cluster receive buffer aliases the pipeline stages
   int dy = 0;  // 1: K boxes after the first stages shared out at run time within the cluster
   int pf = 0;  // k >= 1: the next k stages' weight boxes prefetched into L2 before the PDL wait
+  int rs = 0;  // 1: tcgen05 cluster reduction by per-thread stores at >= 64 tokens (no bulk copies)
   bool valid() const { return variant != 0; }
 };
 
@@ -170,7 +171,8 @@ struct Tactic {
 // with ":d<k>" appended for a late PDL trigger (mma / tc), ":a" for a tcgen05
 // cluster reduction buffer aliased onto the pipeline stages, ":w" for K boxes
 // shared out at run time within a cluster and ":p<k>" for k stages of weight
-// boxes prefetched into L2 before the PDL wait.
+// boxes prefetched into L2 before the PDL wait; ":s" makes a tcgen05 cluster
+// reduction at >= 64 tokens use per-thread stores instead of bulk copies.
 std::string tactic_str(const Tactic& t) {
   char b[96];
   const char* kind = t.variant == kVariantTc ? "tc" : (t.variant == kVariantSk ? "sk" : "mma");
@@ -178,8 +180,8 @@ std::string tactic_str(const Tactic& t) {
   char lt[16] = "", pf[16] = "";
   if (t.lt > 0) snprintf(lt, sizeof lt, ":d%d", t.lt);
   if (t.pf > 0) snprintf(pf, sizeof pf, ":p%d", t.pf);
-  snprintf(b, sizeof b, "%s:r%d:t%d:b%d:s%d:%c%d%s%s%s%s", kind, t.rows, t.tok, t.nbox, t.stages,
-           last, t.cl, lt, pf, t.al ? ":a" : "", t.dy ? ":w" : "");
+  snprintf(b, sizeof b, "%s:r%d:t%d:b%d:s%d:%c%d%s%s%s%s%s", kind, t.rows, t.tok, t.nbox, t.stages,
+           last, t.cl, lt, pf, t.al ? ":a" : "", t.rs ? ":s" : "", t.dy ? ":w" : "");
   return b;
 }
 
@@ -191,7 +193,7 @@ bool tactic_parse(const char* s, Tactic* t) {
   if (s == nullptr || sscanf(s, "%15[^:]:r%d:t%d:b%d:s%d:%c%d%n", kind, &x.rows, &x.tok, &x.nbox,
                              &x.stages, &last, &x.cl, &used) != 7)
     return false;
-  // optional suffixes, in any order, each at most once: ":d<k>", ":p<k>", ":a", ":w"
+  // optional suffixes, in any order, each at most once: ":d<k>", ":p<k>", ":a", ":s", ":w"
   const char* rest = s + used;
   while (*rest != '\0') {
     if (strncmp(rest, ":d", 2) == 0 && x.lt == 0) {
@@ -206,6 +208,9 @@ bool tactic_parse(const char* s, Tactic* t) {
       rest += n2;
     } else if (strncmp(rest, ":a", 2) == 0 && (rest[2] == '\0' || rest[2] == ':') && x.al == 0) {
       x.al = 1;
+      rest += 2;
+    } else if (strncmp(rest, ":s", 2) == 0 && (rest[2] == '\0' || rest[2] == ':') && x.rs == 0) {
+      x.rs = 1;
       rest += 2;
     } else if (strncmp(rest, ":w", 2) == 0 && (rest[2] == '\0' || rest[2] == ':') && x.dy == 0) {
       x.dy = 1;
@@ -227,6 +232,7 @@ bool tactic_parse(const char* s, Tactic* t) {
   if (x.al && x.variant != kVariantTc) return false;
   if (x.dy && x.variant == kVariantSk) return false;
   if (x.pf && (x.variant == kVariantSk || x.dy)) return false;
+  if (x.rs && x.variant != kVariantTc) return false;
   *t = x;
   return true;
 }
@@ -308,7 +314,8 @@ uint64_t env_u64(const char* name, uint64_t dflt) {
   return strtoull(v, nullptr, 10);
 }
 
-const int kTcToks[] = {16, 32, 64, 128, 256};
+const int kTcToks[] = {16, 32, 48, 64, 128, 256};
+const int kSkToks[] = {16, 32, 64};
 const int kMmaToks[] = {8, 16, 32};
 const int kClusters[] = {1, 2, 4, 8, 16};
 
@@ -403,6 +410,8 @@ bool tactic_fits(const skinny_gemm_plan* h, const Tactic& t, int64_t M, std::str
     return no("an aliased receive buffer needs a cluster and stages at least as large");
   if (t.dy && (t.cl < 2 || t.al))
     return no("run-time K sharing (:w) needs a cluster and no aliased receive buffer");
+  if (t.rs && (t.cl < 2 || t.tok < 64))
+    return no("per-thread reduction stores (:s) apply to tcgen05 clusters at >= 64 tokens");
   if (static_cast<int>(tactic_smem(t)) > h->dev->smem_optin)
     return no("shared memory footprint exceeds the per-block limit");
   return true;
@@ -470,6 +479,7 @@ int launch_tactic(skinny_gemm_plan* h, const Tactic& t, const void* x, int64_t l
   p.red_alias = t.al;
   p.dyn_k = t.dy;
   p.l2_pre = t.pf;
+  p.red_stores = t.rs;
   if (h->debug_count > 0) {
     --h->debug_count;
     p.debug_wait = 1;
@@ -526,7 +536,7 @@ int resident_per_sm(const skinny_gemm_plan* h, const Tactic& t) {
   per_sm = std::min(per_sm, regs > 0 ? d.regs_per_sm / regs : per_sm);
   per_sm = std::min(per_sm, d.smem_per_sm / static_cast<int>(tactic_smem(t) + d.smem_reserved));
   const int tmem_cols = t.variant == kVariantSk  ? (2 * t.tok <= 32 ? 32 : (2 * t.tok <= 64 ? 64 : 128))
-                        : t.variant == kVariantTc ? std::max(32, t.tok)
+                        : t.variant == kVariantTc ? (t.tok <= 32 ? 32 : t.tok <= 64 ? 64 : t.tok <= 128 ? 128 : 256)
                                                   : 0;
   if (tmem_cols > 0) per_sm = std::min(per_sm, 512 / tmem_cols);
   return std::max(per_sm, 0);
@@ -574,8 +584,8 @@ std::vector<Tactic> candidates(const skinny_gemm_plan* h, int64_t M) {
   std::vector<Tactic> out;
   std::vector<std::pair<int, int>> vt;  // (variant, token tile)
   for (int variant : {kVariantTc, kVariantMma, kVariantSk}) {
-    const int* toks = variant == kVariantMma ? kMmaToks : kTcToks;
-    const int ntok = variant == kVariantMma ? 3 : (variant == kVariantSk ? 3 : 5);
+    const int* toks = variant == kVariantMma ? kMmaToks : (variant == kVariantSk ? kSkToks : kTcToks);
+    const int ntok = variant == kVariantTc ? 6 : 3;
     for (int i = 0; i < ntok; ++i)
       if (toks[i] >= M) {
         vt.push_back({variant, toks[i]});
@@ -692,6 +702,8 @@ Tactic default_tactic(const skinny_gemm_plan* h, int64_t M) {
     t = with_cluster(Tactic{kVariantMma, 64, 16, 2, 2, 1, 0}, true);
   else if (M <= 32)
     t = with_cluster(Tactic{kVariantTc, 128, 32, 2, 2, 1, 0});
+  else if (M <= 48)
+    t = with_cluster(Tactic{kVariantTc, 128, 48, 1, 3, 1, 0});
   else if (M <= 64)
     t = with_cluster(Tactic{kVariantTc, 128, 64, 1, 3, 1, 0});
   else if (M <= 128)
@@ -1540,6 +1552,23 @@ int skinny_gemm_autotune(skinny_gemm_t h, const int64_t* Ms, int nM, void* strea
       };
       for (size_t c = 0; c < std::min<size_t>(base_timed.size(), 3) && rc == SKG_OK; ++c)
         later_triggers(base_timed[c].second);
+      // The three fastest tcgen05 cluster tactics at >= 64 tokens with per-thread
+      // reduction stores instead of bulk copies.
+      {
+        std::vector<std::pair<double, Tactic>> cur = timed;
+        std::stable_sort(cur.begin(), cur.end(),
+                         [](const auto& a, const auto& b) { return a.first < b.first; });
+        int n_rs = 0;
+        for (size_t c = 0; c < cur.size() && n_rs < 3 && rc == SKG_OK; ++c) {
+          Tactic t = cur[c].second;
+          t.rs = 1;
+          if (t.variant != kVariantTc || !tactic_fits(h, t, M, nullptr)) continue;
+          ++n_rs;
+          double us = 0;
+          rc = time_tactic(t, &us);
+          if (rc == SKG_OK) timed.push_back({us, t});
+        }
+      }
       // The three fastest so far, each with 1, 2 or 4 stages prefetched into L2.
       {
         std::vector<std::pair<double, Tactic>> best3 = timed;

@@ -37,7 +37,8 @@ struct KParams {
                           // through a counter in the cluster's rank-0 CTA (see kDynBytes)
   int32_t l2_pre;         // stages after the first ones whose weight boxes are prefetched
                           // into L2 before the PDL wait (0: none)
-  int32_t pad_;
+  int32_t red_stores;     // tcgen05 clusters, >= 64 tokens: per-thread st.async pushes
+                          // instead of bulk DSMEM copies
   // stream-K kernel only: fp32 partial sums of split tiles and per-tile arrival counters
   float* workspace;       // [gridDim.x][2][TOK][128]
   uint32_t* counters;     // [ceil(N / 128)], zero between launches

@@ -37,7 +37,8 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
   constexpr uint32_t kWBox = ROWS * kBoxRowBytes;
   constexpr uint32_t kXBox = TOK * kBoxRowBytes;
   constexpr uint32_t kStage = stage_bytes(ROWS, TOK, NBOX);
-  constexpr uint32_t kTmemCols = TOK <= 32 ? 32u : static_cast<uint32_t>(TOK);
+  // TMEM is allocated in powers of two of at least 32 columns (48 tokens: 64)
+  constexpr uint32_t kTmemCols = TOK <= 32 ? 32u : TOK <= 64 ? 64u : TOK <= 128 ? 128u : 256u;
   constexpr uint32_t kIdesc = mma_idesc<kFp16>(ROWS, TOK);
   constexpr uint32_t kStageRed = static_cast<uint32_t>(ROWS * TOK) * 4u;
   static_assert(TOK % 16 == 0 && TOK >= 16 && TOK <= 256, "MMA needs N % 16 == 0, N <= 256");
@@ -91,9 +92,9 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
   const int M = min(TOK, p.M - m0);
   // Cluster reduction: for token tiles of 64 and more, bulk DSMEM copies of
   // [TOK][RS] fp32 blocks staged in the idle pipeline buffers (when they are
-  // large enough); for smaller tiles per-thread st.async pushes, which measured
-  // faster there.
-  const bool bulk = csize > 1 && TOK >= 64 &&
+  // large enough), unless the tactic asks for per-thread st.async pushes
+  // (red_stores), which smaller tiles always use.
+  const bool bulk = csize > 1 && TOK >= 64 && p.red_stores == 0 &&
                     static_cast<uint32_t>(S) * kStage >= (alias ? 2u : 1u) * kStageRed;
   // Receive buffer: after the stages, or (aliased) at their start, or right
   // after the bulk path's staging area.
@@ -478,12 +479,14 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
       SKG_TC_ENTRY_R(64, 16, 4, OUTT, OUTCODE, false),                                      \
       SKG_TC_ENTRY_R(64, 32, 1, OUTT, OUTCODE, false), SKG_TC_ENTRY_R(64, 32, 2, OUTT, OUTCODE, false), \
       SKG_TC_ENTRY_R(64, 32, 4, OUTT, OUTCODE, false),                                      \
+      SKG_TC_ENTRY_R(64, 48, 1, OUTT, OUTCODE, false), SKG_TC_ENTRY_R(64, 48, 2, OUTT, OUTCODE, false), \
       SKG_TC_ENTRY_R(64, 64, 1, OUTT, OUTCODE, false), SKG_TC_ENTRY_R(64, 64, 2, OUTT, OUTCODE, false)
 
 #define SKG_TC_ROW(OUTT, OUTCODE)                                                           \
   SKG_TC_ENTRY(16, 1, OUTT, OUTCODE, false), SKG_TC_ENTRY(16, 2, OUTT, OUTCODE, false),     \
       SKG_TC_ENTRY(16, 4, OUTT, OUTCODE, false), SKG_TC_ENTRY(32, 1, OUTT, OUTCODE, false), \
       SKG_TC_ENTRY(32, 2, OUTT, OUTCODE, false), SKG_TC_ENTRY(32, 4, OUTT, OUTCODE, false), \
+      SKG_TC_ENTRY(48, 1, OUTT, OUTCODE, false), SKG_TC_ENTRY(48, 2, OUTT, OUTCODE, false), \
       SKG_TC_ENTRY(64, 1, OUTT, OUTCODE, false), SKG_TC_ENTRY(64, 2, OUTT, OUTCODE, false), \
       SKG_TC_ENTRY(64, 4, OUTT, OUTCODE, false), SKG_TC_ENTRY(128, 1, OUTT, OUTCODE, false), \
       SKG_TC_ENTRY(128, 2, OUTT, OUTCODE, false), SKG_TC_ENTRY(256, 1, OUTT, OUTCODE, false)
@@ -492,6 +495,7 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
 #define SKG_TC_ROW16(OUTT, OUTCODE)                                                         \
   SKG_TC_ENTRY(16, 1, OUTT, OUTCODE, true), SKG_TC_ENTRY(16, 2, OUTT, OUTCODE, true),       \
       SKG_TC_ENTRY(32, 1, OUTT, OUTCODE, true), SKG_TC_ENTRY(32, 2, OUTT, OUTCODE, true),   \
+      SKG_TC_ENTRY(48, 1, OUTT, OUTCODE, true), SKG_TC_ENTRY(48, 2, OUTT, OUTCODE, true),   \
       SKG_TC_ENTRY(64, 1, OUTT, OUTCODE, true), SKG_TC_ENTRY(64, 2, OUTT, OUTCODE, true),   \
       SKG_TC_ENTRY(128, 1, OUTT, OUTCODE, true), SKG_TC_ENTRY(256, 1, OUTT, OUTCODE, true)
 

@@ -94,10 +94,12 @@ def test_tactic_grammar_without_a_gpu(lib_path):
     assert norm("tc:r128:t32:b2:s2:c8:w") == "tc:r128:t32:b2:s2:c8:w"
     assert norm("tc:r128:t64:b2:s2:c8:a:p1:d2") == "tc:r128:t64:b2:s2:c8:d2:p1:a"
     assert norm("mma:r64:t8:b4:s3:c4:p2") == "mma:r64:t8:b4:s3:c4:p2"
+    assert norm("tc:r64:t64:b2:s2:c4:s:a:p2:d1") == "tc:r64:t64:b2:s2:c4:d1:p2:a:s"
+    assert norm("tc:r128:t48:b1:s3:c8") == "tc:r128:t48:b1:s3:c8"
     for bad in ("bogus", "tc:r128:t32:b2:s2", "tc:r128:t32:b2:s2:c8:x", "tc:r128:t32:b2:s2:c8:d0",
                 "tc:r128:t32:b2:s2:c8:d1:d2", "tc:r128:t32:b2:s2:c8:a:a", "mma:r128:t8:b2:s2:c8:a",
                 "sk:r128:t16:b2:s3:p8:d1", "tc:r128:t32:b2:s2:g1", "mma:r128:t8:b2:s2:c8:ab",
                 "sk:r128:t16:b2:s3:p8:w", "mma:r128:t8:b2:s2:c8:w:w", "tc:r128:t32:b2:s2:c8:wa",
                 "mma:r64:t8:b4:s3:c4:p0", "mma:r64:t8:b4:s3:c4:p1:p2", "sk:r128:t16:b2:s3:g1:p1",
-                "mma:r64:t8:b4:s3:c4:p1:w"):
+                "mma:r64:t8:b4:s3:c4:p1:w", "mma:r64:t8:b4:s3:c4:s", "tc:r64:t64:b2:s2:c4:s:s"):
         assert norm(bad) == _native.SKG_EINVAL, bad

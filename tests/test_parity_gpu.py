@@ -58,7 +58,7 @@ def test_split_k_token_tiles(N, out_dtype):
     for M in (4, 8, 16, 32, 48, 64):
         y = run_proj(proj, xd[:M], out_dtype)
         assert_parity(y, ref[:M], s[:M], f"N={N} M={M} {out_dtype} {proj.plan(M)}")
-    assert proj.plan(48).split(":")[2] == "t64"  # M=48 runs on the 64-token tile
+    assert proj.plan(48).split(":")[2] == "t48"  # M=48 runs on the 48-token tile
     proj.check_status()
 
 
@@ -82,6 +82,36 @@ def test_every_candidate_tactic_on_ragged_shape(out_dtype):
             seen.add(t.split(":s")[0])
     proj.check_status()
     assert any(t.startswith("tc:") for t in seen) and any(t.startswith("mma:") for t in seen)
+
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_reduction_by_stores_at_64_tokens(out_dtype):
+    """':s': a tcgen05 cluster reduction at >= 64 tokens sent with per-thread
+    stores instead of bulk copies, on every cluster candidate of the ragged
+    shape and at full size (M = 48 on the 64-token tile too)."""
+    N, K = 656, 1088
+    w, x, ref, s = full_case(N, K, seed=3)
+    proj = skg().Projection(w.to(DEV), out_dtype, use_tactic_file=False)
+    xd = x.to(DEV)
+    n = 0
+    for M in (49, 64):
+        for t in proj.tactics(M):
+            f = t.split(":")
+            if f[0] != "tc" or int(f[5][1:]) < 2 or int(f[2][1:]) < 64:
+                continue
+            proj.set_tactic(M, t + ":s")
+            y = run_proj(proj, xd[:M], out_dtype)
+            assert_parity(y, ref[:M], s[:M], f"M={M} {t}:s")
+            n += 1
+    assert n >= 10, n
+    for Nf in (3584, 6288):
+        w, x, ref, s = full_case(Nf, 7168)
+        p = skg().Projection(w.to(DEV), out_dtype, use_tactic_file=False)
+        for M, t in ((48, "tc:r128:t64:b2:s2:c8:d2:p1:a:s"), (64, "tc:r64:t64:b2:s2:c4:d1:p2:a:s")):
+            p.set_tactic(M, t)
+            y = run_proj(p, x[:M].to(DEV), out_dtype)
+            assert_parity(y, ref[:M], s[:M], f"N={Nf} M={M} {t}")
+        p.close()
 
 
 def test_small_integers_exact_for_every_tactic():
