@@ -1315,6 +1315,34 @@ int skinny_gemm_autotune_overlap(skinny_gemm_t h_main, skinny_gemm_t h_fa, skinn
       }
       step_us = best_us;
     }
+    // Last pass: the main projection's pick with later PDL triggers and with
+    // weight stages prefetched into L2, timed inside the step.
+    if (rc == SKG_OK && h_main->plan[M].variant != kVariantSk) {
+      const Tactic base = h_main->plan[M];
+      double best_us = step_us;
+      Tactic best = base;
+      const int span = late_trigger_span(h_main, base);
+      for (int lt = 0; lt <= 4 && rc == SKG_OK; ++lt)
+        for (int pf : {0, 1, 2}) {
+          Tactic t = base;
+          t.lt = lt;
+          t.pf = t.dy ? 0 : pf;
+          if ((t.lt == base.lt && t.pf == base.pf) || lt > span || t.pf > span ||
+              !tactic_fits(h_main, t, M, nullptr))
+            continue;
+          rc = set_main(M, t);
+          double us = 0;
+          if (rc == SKG_OK) rc = time_step(M, &us);
+          if (rc != SKG_OK) break;
+          if (us < best_us) {
+            best_us = us;
+            best = t;
+          }
+        }
+      const int src = set_main(M, best);
+      if (rc == SKG_OK) rc = src;
+      step_us = best_us;
+    }
     if (rc == SKG_OK) tuned.push_back(M);
     if (log_enabled() && rc == SKG_OK)
       fprintf(stderr, "[skinny_gemm] overlap M=%lld: main %s, F_A %s, step %.3f us\n",
