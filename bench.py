@@ -543,16 +543,20 @@ def host_call_cost(torch, skg, proj, x, out, stream, calls: int = 10000, burst: 
     """Host microseconds per eager call, enqueue time only: bursts of `burst`
     calls (well below the launch queue depth, so no call waits for the GPU),
     each burst timed with perf_counter and followed by a synchronize.  Through
-    the Python binding (Projection.run: shape checks + ctypes) and through the
-    bare C-ABI call (ctypes with prepared arguments)."""
+    the Python binding (Projection.run: shape checks + ctypes), through the
+    bare C-ABI call (ctypes with prepared arguments), and for the host-buffer
+    call (Projection.run_host_async: two copies and the launch enqueued)."""
     lib = skg._native.lib()
     h = proj._h
     xp, op = x.data_ptr(), out.data_ptr()
     M = x.shape[0]
     sp = __import__("ctypes").c_void_p(stream.cuda_stream)
     res = {}
+    xh = x.cpu().pin_memory()
+    oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     for name, fn in (("python_run_us", lambda: proj.run(x, out, stream)),
-                     ("c_abi_run_us", lambda: lib.skinny_gemm_run(h, xp, M, op, sp))):
+                     ("c_abi_run_us", lambda: lib.skinny_gemm_run(h, xp, M, op, sp)),
+                     ("python_run_host_async_us", lambda: proj.run_host_async(xh, oh, stream))):
         fn()
         torch.cuda.synchronize()
         total, n = 0.0, 0

@@ -204,8 +204,11 @@ int skinny_gemm_run_overlap(skinny_gemm_t h_main, skinny_gemm_t h_fa, skinny_gem
  * timed as a CUDA graph of back-to-back launches that rotate over scratch
  * copies of the weight's layout (>= 4.5x the L2 size, so reads come from HBM),
  * i.e. in the steady state of a decode step; the fastest three are timed again
- * with later PDL triggers, and the fastest six with twice the launches and
- * five repetitions decide.  Listed M values with the same candidate list (the
+ * with later PDL triggers, the fastest tcgen05 cluster tactics at >= 64 tokens
+ * with per-thread reduction stores (:s), the fastest six with 1, 2 and 4
+ * stages prefetched into L2 (:p<k>) and, unless the handle was prepared with
+ * SKG_PREPARE_DETERMINISTIC, with run-time K sharing (:w); the fastest six of
+ * all are then timed with twice the launches and five repetitions to decide.  Listed M values with the same candidate list (the
  * same token tiles, e.g. M = 1..8) are tuned together and get one tactic.
  * Synchronizes `stream`;
  * allocates and frees those copies; may grow the handle's workspace; writes

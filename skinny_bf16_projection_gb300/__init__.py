@@ -6,6 +6,7 @@ and stream handles to the library, whose CUDA kernels do all of the work.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 from typing import Iterable, Sequence
 
@@ -23,6 +24,14 @@ _IN_CODES = {torch.bfloat16: _native.SKG_BF16, torch.float16: _native.SKG_FP16}
 
 def library_path() -> str:
     return _native.library_path()
+
+
+_SAME_DEVICE = contextlib.nullcontext()
+
+
+def _device_scope(index: int):
+    """Make device `index` current for a call (a no-op when it already is)."""
+    return _SAME_DEVICE if torch.cuda.current_device() == index else torch.cuda.device(index)
 
 
 def _stream_ptr(stream) -> ctypes.c_void_p:
@@ -74,6 +83,8 @@ class Projection:
         self.N, self.K = weight.shape
         self.out_dtype = out_dtype
         self.device = weight.device
+        self._dev_index = weight.device.index if weight.device.index is not None else \
+            torch.cuda.current_device()
 
     # ---------------------------------------------------------------- running
     def run(self, x: torch.Tensor, out: torch.Tensor, stream=None,
@@ -115,7 +126,7 @@ class Projection:
     def run_host(self, x_host: torch.Tensor, out_host: torch.Tensor, stream=None) -> torch.Tensor:
         """End-to-end call with host (ideally pinned) buffers; synchronizes the stream."""
         self._check_host(x_host, out_host)
-        with torch.cuda.device(self.device):
+        with _device_scope(self._dev_index):
             _native.check(self._lib.skinny_gemm_run_host(
                 self._h, x_host.data_ptr(), x_host.shape[0], out_host.data_ptr(),
                 _stream_ptr(stream)))
@@ -125,7 +136,7 @@ class Projection:
         """Enqueue copy-in, projection and copy-out on the stream without waiting
         (pinned host buffers; synchronize the stream before reading out_host)."""
         self._check_host(x_host, out_host)
-        with torch.cuda.device(self.device):
+        with _device_scope(self._dev_index):
             _native.check(self._lib.skinny_gemm_run_host_async(
                 self._h, x_host.data_ptr(), x_host.shape[0], out_host.data_ptr(),
                 _stream_ptr(stream)))

@@ -1597,14 +1597,15 @@ int skinny_gemm_autotune(skinny_gemm_t h, const int64_t* Ms, int nM, void* strea
           if (rc == SKG_OK) timed.push_back({us, t});
         }
       }
-      // The three fastest so far, each with 1, 2 or 4 stages prefetched into L2.
+      // The six fastest so far, each with 1, 2 or 4 stages prefetched into L2 (a
+      // tactic that is not among the fastest without prefetch can gain the most).
       {
-        std::vector<std::pair<double, Tactic>> best3 = timed;
-        std::stable_sort(best3.begin(), best3.end(),
+        std::vector<std::pair<double, Tactic>> best6 = timed;
+        std::stable_sort(best6.begin(), best6.end(),
                          [](const auto& a, const auto& b) { return a.first < b.first; });
-        for (size_t c = 0; c < std::min<size_t>(best3.size(), 3) && rc == SKG_OK; ++c)
+        for (size_t c = 0; c < std::min<size_t>(best6.size(), 6) && rc == SKG_OK; ++c)
           for (int pf : {1, 2, 4}) {
-            Tactic t = best3[c].second;
+            Tactic t = best6[c].second;
             if (t.variant == kVariantSk || late_trigger_span(h, t) < pf) break;
             t.pf = pf;
             double us = 0;
