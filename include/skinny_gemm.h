@@ -203,10 +203,10 @@ int skinny_gemm_run_overlap(skinny_gemm_t h_main, skinny_gemm_t h_fa, skinny_gem
  * autotune_kda_qkvg: autotune before CUDA graph capture).  Each candidate is
  * timed as a CUDA graph of back-to-back launches that rotate over scratch
  * copies of the weight's layout (>= 4.5x the L2 size, so reads come from HBM),
- * i.e. in the steady state of a decode step; the fastest three are timed again
- * with later PDL triggers, the fastest tcgen05 cluster tactics at >= 64 tokens
- * with per-thread reduction stores (:s), the fastest six with 1, 2 and 4
- * stages prefetched into L2 (:p<k>) and, unless the handle was prepared with
+ * i.e. in the steady state of a decode step; the fastest six are timed again
+ * with every combination of a later PDL trigger (:d1-:d4) and an L2 prefetch
+ * depth (:p1, :p2, :p4), tcgen05 cluster tactics at >= 64 tokens also with
+ * per-thread reduction stores (:s), and, unless the handle was prepared with
  * SKG_PREPARE_DETERMINISTIC, with run-time K sharing (:w); the fastest six of
  * all are then timed with twice the launches and five repetitions to decide.  Listed M values with the same candidate list (the
  * same token tiles, e.g. M = 1..8) are tuned together and get one tactic.

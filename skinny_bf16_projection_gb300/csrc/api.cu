@@ -622,16 +622,17 @@ std::vector<Tactic> candidates(const skinny_gemm_plan* h, int64_t M) {
           }
           out.push_back(t);
           // tcgen05 clusters: the variant whose receive buffer aliases the stages,
-          // when that lets more CTAs share an SM (it waits for the whole cluster's
-          // MMAs before reducing, so it only pays off through residency).
+          // when that lets more CTAs share an SM, and always at >= 48 tokens,
+          // where it timed fastest on the 3584x7168 weight at equal residency (it
+          // waits for the whole cluster's MMAs before reducing).
           if (variant == kVariantTc && t.cl > 1) {
             Tactic ta = t;
             ta.al = 1;
             const int per = h->dev->smem_per_sm;
             const int rsv = h->dev->smem_reserved;
             if (tactic_fits(h, ta, M, nullptr) &&
-                per / static_cast<int>(tactic_smem(ta) + rsv) >
-                    per / static_cast<int>(tactic_smem(t) + rsv) &&
+                (tok >= 48 || per / static_cast<int>(tactic_smem(ta) + rsv) >
+                                  per / static_cast<int>(tactic_smem(t) + rsv)) &&
                 active_clusters(h, ta) > 0)
               out.push_back(ta);
           }
@@ -1561,9 +1562,12 @@ int skinny_gemm_autotune(skinny_gemm_t h, const int64_t* Ms, int nM, void* strea
       if (rc != SKG_OK) break;
       timed.push_back({us, t});
     }
-    // Phase 2: the fastest few again with later PDL triggers; unless the handle
-    // is deterministic, the six fastest cluster tactics also with run-time K
-    // sharing (:w), and the best two of those with later triggers too.
+    // Phase 2: the six fastest of phase 1, each with every later PDL trigger
+    // (:d1-:d4) and L2 prefetch depth (:p1, :p2, :p4) and their combinations,
+    // tcgen05 cluster tactics at >= 64 tokens also with per-thread reduction
+    // stores (:s) (a tactic that is not the fastest alone can gain the most);
+    // unless the handle is deterministic, the six fastest cluster tactics also
+    // with run-time K sharing (:w), and the best two of those with later triggers.
     if (rc == SKG_OK) {
       std::stable_sort(timed.begin(), timed.end(),
                        [](const auto& a, const auto& b) { return a.first < b.first; });
@@ -1578,41 +1582,24 @@ int skinny_gemm_autotune(skinny_gemm_t h, const int64_t* Ms, int nM, void* strea
           if (rc == SKG_OK) timed.push_back({us, t});
         }
       };
-      for (size_t c = 0; c < std::min<size_t>(base_timed.size(), 3) && rc == SKG_OK; ++c)
-        later_triggers(base_timed[c].second);
-      // The three fastest tcgen05 cluster tactics at >= 64 tokens with per-thread
-      // reduction stores instead of bulk copies.
-      {
-        std::vector<std::pair<double, Tactic>> cur = timed;
-        std::stable_sort(cur.begin(), cur.end(),
-                         [](const auto& a, const auto& b) { return a.first < b.first; });
-        int n_rs = 0;
-        for (size_t c = 0; c < cur.size() && n_rs < 3 && rc == SKG_OK; ++c) {
-          Tactic t = cur[c].second;
-          t.rs = 1;
-          if (t.variant != kVariantTc || !tactic_fits(h, t, M, nullptr)) continue;
-          ++n_rs;
-          double us = 0;
-          rc = time_tactic(t, &us);
-          if (rc == SKG_OK) timed.push_back({us, t});
-        }
-      }
-      // The six fastest so far, each with 1, 2 or 4 stages prefetched into L2 (a
-      // tactic that is not among the fastest without prefetch can gain the most).
-      {
-        std::vector<std::pair<double, Tactic>> best6 = timed;
-        std::stable_sort(best6.begin(), best6.end(),
-                         [](const auto& a, const auto& b) { return a.first < b.first; });
-        for (size_t c = 0; c < std::min<size_t>(best6.size(), 6) && rc == SKG_OK; ++c)
-          for (int pf : {1, 2, 4}) {
-            Tactic t = best6[c].second;
-            if (t.variant == kVariantSk || late_trigger_span(h, t) < pf) break;
-            t.pf = pf;
-            double us = 0;
-            rc = time_tactic(t, &us);
-            if (rc == SKG_OK) timed.push_back({us, t});
-            if (rc != SKG_OK) break;
-          }
+      for (size_t c = 0; c < std::min<size_t>(base_timed.size(), 6) && rc == SKG_OK; ++c) {
+        const Tactic t0 = base_timed[c].second;
+        if (t0.variant == kVariantSk) continue;
+        const int span = late_trigger_span(h, t0);
+        for (int rs = 0; rs <= 1 && rc == SKG_OK; ++rs)
+          for (int lt = 0; lt <= 4 && lt <= span && rc == SKG_OK; ++lt)
+            for (int pf : {0, 1, 2, 4}) {
+              Tactic t = t0;
+              t.rs = rs;
+              t.lt = lt;
+              t.pf = pf;
+              if ((rs == 0 && lt == 0 && pf == 0) || pf > span) continue;
+              if (rs == 1 && !tactic_fits(h, t, M, nullptr)) break;
+              double us = 0;
+              rc = time_tactic(t, &us);
+              if (rc != SKG_OK) break;
+              timed.push_back({us, t});
+            }
       }
       if (!h->deterministic) {
         std::vector<std::pair<double, Tactic>> shared;
