@@ -223,8 +223,12 @@ int skinny_gemm_autotune(skinny_gemm_t h, const int64_t* Ms, int nM, void* strea
  * tactics of F_A, then of the main projection, then of F_A again are each
  * timed inside the whole step (main projection rotating over scratch copies of
  * its weight, F_A -> F_B chain on a high-priority aux stream, fork/join by
- * events), as a CUDA graph of back-to-back steps, and the tactic with the
- * shortest step is installed in h_fa's / h_main's plan.  (A tactic that is
+ * events), as a CUDA graph of back-to-back steps; the four fastest of each
+ * pass are timed again with twice the steps and five replays, and the
+ * fastest of those is installed in h_fa's / h_main's plan.  A last pass times
+ * the main pick with every later PDL trigger (:d1-:d4) and L2 prefetch depth
+ * (:p1, :p2) inside the step and keeps the fastest of the three best timed
+ * the longer way.  (A tactic that is
  * fastest alone can be slow next to a grid that fills the GPU; the main
  * projection's step-tuned plan may be slower when it runs alone.)  F_B keeps
  * its plan.  Same rules as skinny_gemm_autotune: synchronizes `stream`,
