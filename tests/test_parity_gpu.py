@@ -82,6 +82,13 @@ def test_every_candidate_tactic_on_ragged_shape(out_dtype):
             seen.add(t.split(":s")[0])
     proj.check_status()
     assert any(t.startswith("tc:") for t in seen) and any(t.startswith("mma:") for t in seen)
+    # at >= 48 tokens every tcgen05 cluster candidate is also listed with its
+    # receive buffer aliased onto the stages (where that fits shared memory)
+    for M in (48, 64):
+        cands = set(proj.tactics(M))
+        plain = [t for t in cands if t.startswith("tc:") and int(t.split(":c")[1].split(":")[0]) > 1
+                 and not t.endswith(":a")]
+        assert plain and any(t + ":a" in cands for t in plain), sorted(cands)[:8]
 
 
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
