@@ -57,7 +57,8 @@ enum skinny_gemm_status {
   SKG_EDEVICE = 4,         /* current device is not sm_103 */
   SKG_ECUDA = 5,           /* a CUDA runtime/driver call failed */
   SKG_ECAPTURING = 6,      /* prepare/autotune called while the stream captures */
-  SKG_ETIMEOUT = 7         /* a device-side bounded wait expired (watchdog) */
+  SKG_ETIMEOUT = 7,        /* a device-side bounded wait expired (watchdog) */
+  SKG_ECHECK = 8           /* checked build only: a device-side bounds check failed */
 };
 
 /* Flags for skinny_gemm_prepare_ex. */
@@ -276,7 +277,9 @@ int skinny_gemm_list_tactics(skinny_gemm_t h, int64_t M, char* buf, size_t len);
 
 /* Synchronize `stream`, then read and clear the handle's device status word.
  * Returns SKG_OK, SKG_ETIMEOUT if a kernel's bounded wait expired since the
- * last check, or ECUDA.  Not capturable. */
+ * last check, SKG_ECHECK if (in the checked build, libskinny_gemm_checked.so,
+ * compiled with SKG_DEVICE_CHECKS) an access failed its bounds test and was
+ * skipped (the message names the access), or ECUDA.  Not capturable. */
 int skinny_gemm_check_status(skinny_gemm_t h, void* stream);
 
 /* Debug aid for the watchdog: the next `count` launches on this handle

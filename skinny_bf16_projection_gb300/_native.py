@@ -14,9 +14,9 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libskinny_
 # enum skinny_gemm_dtype / skinny_gemm_status (mirrors include/skinny_gemm.h)
 SKG_BF16, SKG_FP16, SKG_FP32 = 0, 1, 2
 SKG_OK, SKG_EINVAL, SKG_EALIGN, SKG_EUNSUPPORTED_M = 0, 1, 2, 3
-SKG_EDEVICE, SKG_ECUDA, SKG_ECAPTURING, SKG_ETIMEOUT = 4, 5, 6, 7
+SKG_EDEVICE, SKG_ECUDA, SKG_ECAPTURING, SKG_ETIMEOUT, SKG_ECHECK = 4, 5, 6, 7, 8
 STATUS_NAMES = {0: "OK", 1: "EINVAL", 2: "EALIGN", 3: "EUNSUPPORTED_M", 4: "EDEVICE",
-                5: "ECUDA", 6: "ECAPTURING", 7: "ETIMEOUT"}
+                5: "ECUDA", 6: "ECAPTURING", 7: "ETIMEOUT", 8: "ECHECK"}
 MAX_M = 256
 
 # (name, restype, argtypes) for every function the header declares.

@@ -1712,6 +1712,9 @@ int skinny_gemm_check_status(skinny_gemm_t h, void* stream) {
     cudaMemset(h->status, 0, sizeof v);
     // a kernel that gave up may have left split-tile counters mid-count
     if (h->counters) cudaMemset(h->counters, 0, h->counters_bytes);
+    if ((v & 0xffff0000u) == kStatusCheck)
+      return fail(SKG_ECHECK, "device check failed: access %u out of bounds (code 0x%08x)",
+                  v & 0xffffu, v);
     return fail(SKG_ETIMEOUT, "device watchdog: bounded wait expired (code 0x%08x)", v);
   }
   return ok();

@@ -31,6 +31,30 @@ __device__ __forceinline__ void report_status(uint32_t* status, uint32_t code) {
   if (status != nullptr) atomicCAS(status, 0u, code);
 }
 
+// Checked build (-DSKG_DEVICE_CHECKS=1): an access guarded by skg_check is
+// tested first; a failed test records kStatusCheck | site (first error wins)
+// and the caller skips the access.  In the normal build the test compiles away.
+#ifndef SKG_DEVICE_CHECKS
+#define SKG_DEVICE_CHECKS 0
+#endif
+__device__ __forceinline__ bool skg_check(bool ok, uint32_t* status, uint32_t site) {
+  if constexpr (SKG_DEVICE_CHECKS != 0) {
+    if (!ok) report_status(status, kStatusCheck | site);
+    return ok;
+  } else {
+    (void)ok;
+    (void)status;
+    (void)site;
+    return true;
+  }
+}
+// Bytes of dynamic shared memory this launch was given.
+__device__ __forceinline__ uint32_t dynamic_smem_bytes() {
+  uint32_t r;
+  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(r));
+  return r;
+}
+
 // Barrier among `nthreads` threads (whole warps) of the CTA, separate from __syncthreads.
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -265,6 +289,7 @@ __device__ __forceinline__ float from_out(__half v) { return __half2float(v); }
 // the residual joins the fp32 sum before the single rounding to the output type.
 template <typename OutT>
 __device__ __forceinline__ void store_out(const KParams& p, int t, int n, float v) {
+  if (!skg_check(t >= 0 && t < p.M && n >= 0 && n < p.N, p.status, kCheckOut)) return;
   if (p.residual != nullptr)
     v += from_out(static_cast<const OutT*>(p.residual)[static_cast<int64_t>(t) * p.ldr + n]);
   static_cast<OutT*>(p.out)[static_cast<int64_t>(t) * p.ldo + n] = to_out<OutT>(v);
@@ -301,6 +326,7 @@ __device__ __forceinline__ float2 unpack2<__half>(uint32_t u) {
 // that out (and residual) rows are 16-byte aligned at n and n + 8 <= N.
 template <typename OutT>
 __device__ __forceinline__ void store_out8(const KParams& p, int t, int n, const float (&v)[8]) {
+  if (!skg_check(t >= 0 && t < p.M && n >= 0 && n + 8 <= p.N, p.status, kCheckOut)) return;
   float w[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) w[j] = v[j];

@@ -18,6 +18,23 @@ enum : uint32_t {
   kStatusTimeoutRecv = 0x10000004u,   // waiting for cluster peers' partial sums
   kStatusTimeoutDebug = 0x10000005u,  // injected watchdog self-test
   kStatusTimeoutDrain = 0x10000006u,  // final drain of in-flight copies
+  // checked build (SKG_DEVICE_CHECKS): an access failed its bounds test and was
+  // skipped; the low 16 bits name the access (kCheck* below)
+  kStatusCheck = 0x20000000u,
+};
+
+// Accesses tested in a checked build.
+enum : uint32_t {
+  kCheckTmaW = 1,       // weight box destination inside the pipeline stages
+  kCheckTmaX = 2,       // x box destination inside the pipeline stages
+  kCheckMmaOperand = 3, // MMA / ldmatrix operand inside its stage box
+  kCheckTmem = 4,       // TMEM column range inside the allocation
+  kCheckRedLocal = 5,   // write into this CTA's receive / staging buffer
+  kCheckRedRemote = 6,  // push into a peer's receive buffer
+  kCheckRedRead = 7,    // reduction read of the receive buffer
+  kCheckOut = 8,        // output element inside [M, N]
+  kCheckWorkspace = 9,  // stream-K partial-sum slot / tile counter
+  kCheckBulk = 10,      // bulk DSMEM copy source / destination range
 };
 
 struct KParams {

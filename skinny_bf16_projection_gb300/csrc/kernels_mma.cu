@@ -42,6 +42,8 @@ __global__ void __launch_bounds__(160) skinny_mma_kernel(const __grid_constant__
   uint8_t* const gbase = smem_raw + (base - raw);
   const int S = p.stages;
   const uint32_t red = base + static_cast<uint32_t>(S) * kStage;
+  const uint32_t stages_end = red;  // (checked build only)
+  const uint32_t red_words = static_cast<uint32_t>(ROWS * TOK);
   float* const red_g = reinterpret_cast<float*>(gbase + static_cast<uint32_t>(S) * kStage);
   const uint32_t bars = red + red_bytes(ROWS, TOK);
   const uint32_t recv_bar = bars + 8u * (2 * S) + 8u;
@@ -129,7 +131,9 @@ __global__ void __launch_bounds__(160) skinny_mma_kernel(const __grid_constant__
         const uint32_t st = base + static_cast<uint32_t>(pro) * kStage;
         mbar_arrive_expect_tx(full_bar(pro), nbi * (kWBox + kXBox));
         for (int b = 0; b < nbi; ++b)
-          tma_load_2d_hint(st + b * kWBox, &wmap, (b0 + b) * kBoxK, n0, full_bar(pro), policy);
+          if (skg_check(st + (b + 1) * kWBox <= stages_end && ((b0 + b) * kBoxK) % 8 == 0, p.status,
+                        kCheckTmaW))
+            tma_load_2d_hint(st + b * kWBox, &wmap, (b0 + b) * kBoxK, n0, full_bar(pro), policy);
       }
       // The weight boxes of the next l2_pre stages go to L2 now: these requests
       // queue behind the previous grid's last loads and are served while it
@@ -154,7 +158,8 @@ __global__ void __launch_bounds__(160) skinny_mma_kernel(const __grid_constant__
         const int nbi = fixed_count(it, b0);
         const uint32_t st = base + static_cast<uint32_t>(it) * kStage + NBOX * kWBox;
         for (int b = 0; b < nbi; ++b)
-          tma_load_2d(st + b * kXBox, &xmap, (b0 + b) * kBoxK, 0, full_bar(it));
+          if (skg_check(st + (b + 1) * kXBox <= stages_end, p.status, kCheckTmaX))
+            tma_load_2d(st + b * kXBox, &xmap, (b0 + b) * kBoxK, 0, full_bar(it));
       }
     }
     __syncwarp();
@@ -195,9 +200,12 @@ __global__ void __launch_bounds__(160) skinny_mma_kernel(const __grid_constant__
         const uint32_t st = base + static_cast<uint32_t>(s) * kStage;
         mbar_arrive_expect_tx(full_bar(s), nbi * (kWBox + kXBox));
         for (int b = 0; b < nbi; ++b)
-          tma_load_2d_hint(st + b * kWBox, &wmap, (b0 + b) * kBoxK, n0, full_bar(s), policy);
+          if (skg_check(st + (b + 1) * kWBox <= stages_end && ((b0 + b) * kBoxK) % 8 == 0, p.status,
+                        kCheckTmaW))
+            tma_load_2d_hint(st + b * kWBox, &wmap, (b0 + b) * kBoxK, n0, full_bar(s), policy);
         for (int b = 0; b < nbi; ++b)
-          tma_load_2d(st + NBOX * kWBox + b * kXBox, &xmap, (b0 + b) * kBoxK, 0, full_bar(s));
+          if (skg_check(st + NBOX * kWBox + (b + 1) * kXBox <= stages_end, p.status, kCheckTmaX))
+            tma_load_2d(st + NBOX * kWBox + b * kXBox, &xmap, (b0 + b) * kBoxK, 0, full_bar(s));
         if (dyn) next_b0 = static_cast<int>(atom_add_cluster_u32(counter, NBOX));
       }
       n_armed = it;
@@ -232,14 +240,18 @@ __global__ void __launch_bounds__(160) skinny_mma_kernel(const __grid_constant__
           for (int mt = 0; mt < MT; ++mt) {
             const uint32_t row = static_cast<uint32_t>(row_base + mt * 16) + (lane & 15u);
             const uint32_t chunk = static_cast<uint32_t>(2 * j) + (lane >> 4);
-            ldsm_x4(wb + row * 128u + ((chunk ^ (row & 7u)) << 4), a[mt][0], a[mt][1], a[mt][2],
-                    a[mt][3]);
+            const uint32_t aaddr = wb + row * 128u + ((chunk ^ (row & 7u)) << 4);
+            // (a failing lane reads the box start instead, so the collective stays warp-wide)
+            const bool aok = skg_check(aaddr >= wb && aaddr + 16u <= wb + kWBox, p.status, kCheckMmaOperand);
+            ldsm_x4(aok ? aaddr : wb, a[mt][0], a[mt][1], a[mt][2], a[mt][3]);
           }
           if constexpr (TOK == 8) {
             const uint32_t tr = lane & 7u;
             const uint32_t chunk = static_cast<uint32_t>(2 * j) + ((lane >> 3) & 1u);
             uint32_t b0, b1;
-            ldsm_x2(xb + tr * 128u + ((chunk ^ (tr & 7u)) << 4), b0, b1);
+            const uint32_t baddr = xb + tr * 128u + ((chunk ^ (tr & 7u)) << 4);
+            const bool bok = skg_check(baddr >= xb && baddr + 16u <= xb + kXBox, p.status, kCheckMmaOperand);
+            ldsm_x2(bok ? baddr : xb, b0, b1);
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) mma_16816<kFp16>(acc[mt][0], a[mt], b0, b1);
           } else {
@@ -248,7 +260,10 @@ __global__ void __launch_bounds__(160) skinny_mma_kernel(const __grid_constant__
               const uint32_t tr = static_cast<uint32_t>(np * 16) + ((lane >> 4) << 3) + (lane & 7u);
               const uint32_t chunk = static_cast<uint32_t>(2 * j) + ((lane >> 3) & 1u);
               uint32_t b00, b01, b10, b11;
-              ldsm_x4(xb + tr * 128u + ((chunk ^ (tr & 7u)) << 4), b00, b01, b10, b11);
+              const uint32_t baddr = xb + tr * 128u + ((chunk ^ (tr & 7u)) << 4);
+              const bool bok =
+                  skg_check(baddr >= xb && baddr + 16u <= xb + kXBox, p.status, kCheckMmaOperand);
+              ldsm_x4(bok ? baddr : xb, b00, b01, b10, b11);
 #pragma unroll
               for (int mt = 0; mt < MT; ++mt) {
                 mma_16816<kFp16>(acc[mt][2 * np], a[mt], b00, b01);
@@ -282,8 +297,10 @@ __global__ void __launch_bounds__(160) skinny_mma_kernel(const __grid_constant__
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             const int t = nt * 8 + 2 * q;
-            if (t < M) red_g[(rank * TOK + t) * RS + rs] = acc[mt][nt][2 * h];
-            if (t + 1 < M) red_g[(rank * TOK + t + 1) * RS + rs] = acc[mt][nt][2 * h + 1];
+            const uint32_t i0 = static_cast<uint32_t>((rank * TOK + t) * RS + rs);
+            if (!skg_check(i0 + static_cast<uint32_t>(RS) < red_words, p.status, kCheckRedLocal)) continue;
+            if (t < M) red_g[i0] = acc[mt][nt][2 * h];
+            if (t + 1 < M) red_g[i0 + RS] = acc[mt][nt][2 * h + 1];
           }
         } else {
           const uint32_t raddr = mapa_shared(red + ((rank * TOK) * RS + rs) * 4u, owner);
@@ -291,6 +308,10 @@ __global__ void __launch_bounds__(160) skinny_mma_kernel(const __grid_constant__
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             const int t = nt * 8 + 2 * q;
+            if (!skg_check(owner < csize &&
+                               static_cast<uint32_t>((rank * TOK + t + 1) * RS + rs) < red_words,
+                           p.status, kCheckRedRemote))
+              continue;
             if (t < M) st_async_b32(raddr + static_cast<uint32_t>(t * RS * 4), acc[mt][nt][2 * h], rbar);
             if (t + 1 < M)
               st_async_b32(raddr + static_cast<uint32_t>((t + 1) * RS * 4), acc[mt][nt][2 * h + 1],
@@ -316,6 +337,9 @@ __global__ void __launch_bounds__(160) skinny_mma_kernel(const __grid_constant__
     const int rs2 = idx % RS;
     const int t = idx / RS;
     float sum = 0.0f;
+    if (!skg_check(static_cast<uint32_t>(((csize - 1) * TOK + t) * RS + rs2) < red_words, p.status,
+                   kCheckRedRead))
+      continue;
     for (uint32_t k = 0; k < csize; ++k) sum += red_g[(k * TOK + t) * RS + rs2];
     const int n = nbase + rs2;
     if (n < p.N) store_out<OutT>(p, t, n, sum);

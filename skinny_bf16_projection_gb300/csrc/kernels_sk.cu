@@ -91,6 +91,7 @@ __global__ void __launch_bounds__(192) skinny_sk_kernel(const __grid_constant__ 
   uint8_t* const gbase = smem_raw + (base - raw);
   const int S = p.stages;
   const uint32_t bars = base + static_cast<uint32_t>(S) * kStage;
+  const uint32_t stages_end = bars;  // (checked build only)
   const uint32_t tfull_bar = bars + 8u * (2 * S);     // [2]
   const uint32_t tempty_bar = tfull_bar + 16u;        // [2]
   const uint32_t dbg_bar = tempty_bar + 16u;
@@ -165,7 +166,9 @@ __global__ void __launch_bounds__(192) skinny_sk_kernel(const __grid_constant__ 
         const uint32_t st = base + static_cast<uint32_t>(it) * kStage;
         mbar_arrive_expect_tx(full_bar(it), n * (kWBox + kXBox));
         for (int b = 0; b < n; ++b)
-          tma_load_2d_hint(st + b * kWBox, &wmap, (k + b) * kBoxK, t * ROWS, full_bar(it), policy);
+          if (skg_check(st + (b + 1) * kWBox <= stages_end && ((k + b) * kBoxK) % 8 == 0, p.status,
+                        kCheckTmaW))
+            tma_load_2d_hint(st + b * kWBox, &wmap, (k + b) * kBoxK, t * ROWS, full_bar(it), policy);
       }
       // Let the next kernel on the stream launch now: its CTAs can prefetch their
       // own weight tiles while this grid streams (they still wait for our
@@ -176,7 +179,8 @@ __global__ void __launch_bounds__(192) skinny_sk_kernel(const __grid_constant__ 
       for (int it = 0; it < pro && sx.next(t, k, n); ++it) {
         const uint32_t st = base + static_cast<uint32_t>(it) * kStage + NBOX * kWBox;
         for (int b = 0; b < n; ++b)
-          tma_load_2d(st + b * kXBox, &xmap, (k + b) * kBoxK, 0, full_bar(it));
+          if (skg_check(st + (b + 1) * kXBox <= stages_end, p.status, kCheckTmaX))
+            tma_load_2d(st + b * kXBox, &xmap, (k + b) * kBoxK, 0, full_bar(it));
       }
       for (int it = pro; si.next(t, k, n); ++it) {
         const int s = it % S;
@@ -186,9 +190,12 @@ __global__ void __launch_bounds__(192) skinny_sk_kernel(const __grid_constant__ 
         const uint32_t st = base + static_cast<uint32_t>(s) * kStage;
         mbar_arrive_expect_tx(full_bar(s), n * (kWBox + kXBox));
         for (int b = 0; b < n; ++b)
-          tma_load_2d_hint(st + b * kWBox, &wmap, (k + b) * kBoxK, t * ROWS, full_bar(s), policy);
+          if (skg_check(st + (b + 1) * kWBox <= stages_end && ((k + b) * kBoxK) % 8 == 0, p.status,
+                        kCheckTmaW))
+            tma_load_2d_hint(st + b * kWBox, &wmap, (k + b) * kBoxK, t * ROWS, full_bar(s), policy);
         for (int b = 0; b < n; ++b)
-          tma_load_2d(st + NBOX * kWBox + b * kXBox, &xmap, (k + b) * kBoxK, 0, full_bar(s));
+          if (skg_check(st + NBOX * kWBox + (b + 1) * kXBox <= stages_end, p.status, kCheckTmaX))
+            tma_load_2d(st + NBOX * kWBox + b * kXBox, &xmap, (k + b) * kBoxK, 0, full_bar(s));
       }
     }
     __syncwarp();
@@ -246,7 +253,13 @@ __global__ void __launch_bounds__(192) skinny_sk_kernel(const __grid_constant__ 
 #pragma unroll
       for (int cc = 0; cc < TOK / 16; ++cc) {
         float t16[16];
-        tmem_ld_32x32b_x16(taddr + static_cast<uint32_t>(cc * 16), t16);
+        // (acc and cc are the same in every lane: the collective load stays warp-wide)
+        if (skg_check(acc * TOK + cc * 16 + 16 <= static_cast<int>(kTmemCols), p.status, kCheckTmem)) {
+          tmem_ld_32x32b_x16(taddr + static_cast<uint32_t>(cc * 16), t16);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) t16[i] = 0.0f;
+        }
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[cc * 16 + i] = t16[i];
       }
@@ -266,9 +279,12 @@ __global__ void __launch_bounds__(192) skinny_sk_kernel(const __grid_constant__ 
       // Split tile: publish this part, count arrivals, the last one finishes.
       const int slot_self = c * 2 + (t == first_tile ? 0 : 1);
       float* const ws_self = p.workspace + static_cast<int64_t>(slot_self) * TOK * ROWS;
+      const bool ws_ok = skg_check(slot_self >= 0 && slot_self < 2 * static_cast<int>(gridDim.x) &&
+                                       row < ROWS && t >= 0 && t < ntiles,
+                                   p.status, kCheckWorkspace);
 #pragma unroll
       for (int tk = 0; tk < TOK; ++tk)
-        if (tk < M) __stcg(ws_self + tk * ROWS + row, v[tk]);
+        if (tk < M && ws_ok) __stcg(ws_self + tk * ROWS + row, v[tk]);
       named_barrier_sync(1, 128);  // all parts of this CTA written before the release below
       const int c_first = cta_of_unit(static_cast<int64_t>(t) * kb, U, G);
       const int c_last = cta_of_unit(static_cast<int64_t>(t + 1) * kb - 1, U, G);
@@ -296,7 +312,9 @@ __global__ void __launch_bounds__(192) skinny_sk_kernel(const __grid_constant__ 
             for (int q = 0; q < kPB; ++q) {
               const int cq = c_first + min(q0 + q, parts - 1);
               const int first_q = static_cast<int>(static_cast<int64_t>(cq) * U / G) / kb;
-              const int slot = cq * 2 + (t == first_q ? 0 : 1);
+              int slot = cq * 2 + (t == first_q ? 0 : 1);
+              if (!skg_check(slot >= 0 && slot < 2 * static_cast<int>(gridDim.x), p.status, kCheckWorkspace))
+                slot = 0;
               base_q[q] = p.workspace + static_cast<int64_t>(slot) * TOK * ROWS;
             }
             float4 pv[kIB][kPB];
@@ -307,7 +325,9 @@ __global__ void __launch_bounds__(192) skinny_sk_kernel(const __grid_constant__ 
 #pragma unroll
               for (int q = 0; q < kPB; ++q) {
                 pv[ii][q] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                if (item < items && q0 + q < parts) pv[ii][q] = ld_cg_f32x4(base_q[q] + off);
+                if (item < items && q0 + q < parts &&
+                    skg_check(off >= 0 && off + 4 <= TOK * ROWS, p.status, kCheckWorkspace))
+                  pv[ii][q] = ld_cg_f32x4(base_q[q] + off);
               }
             }
 #pragma unroll

@@ -55,6 +55,7 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
   // the cluster barrier that each CTA arrives at from that point on.
   const bool alias = p.red_alias != 0 && csize > 1;
   const uint32_t stages_end = base + static_cast<uint32_t>(S) * kStage;
+  const uint32_t smem_end = raw + dynamic_smem_bytes();  // (checked build only)
   const uint32_t bars = stages_end + (csize > 1 && !alias ? tc_red_bytes(TOK, ROWS) : 0u);
   const uint32_t done_bar = bars + 8u * (2 * S);
   const uint32_t recv_bar = done_bar + 8u;
@@ -165,7 +166,9 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
         const uint32_t st = base + static_cast<uint32_t>(pro) * kStage;
         mbar_arrive_expect_tx(full_bar(pro), nbi * (kWBox + kXBox));
         for (int b = 0; b < nbi; ++b)
-          tma_load_2d_hint(st + b * kWBox, &wmap, (b0 + b) * kBoxK, n0, full_bar(pro), policy);
+          if (skg_check(st + (b + 1) * kWBox <= stages_end && ((b0 + b) * kBoxK) % 8 == 0, p.status,
+                        kCheckTmaW))
+            tma_load_2d_hint(st + b * kWBox, &wmap, (b0 + b) * kBoxK, n0, full_bar(pro), policy);
       }
       // The weight boxes of the next l2_pre stages go to L2 now: these requests
       // queue behind the previous grid's last loads and are served while it
@@ -190,7 +193,8 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
         const int nbi = fixed_count(it, b0);
         const uint32_t st = base + static_cast<uint32_t>(it) * kStage + NBOX * kWBox;
         for (int b = 0; b < nbi; ++b)
-          tma_load_2d(st + b * kXBox, &xmap, (b0 + b) * kBoxK, m0, full_bar(it));
+          if (skg_check(st + (b + 1) * kXBox <= stages_end, p.status, kCheckTmaX))
+            tma_load_2d(st + b * kXBox, &xmap, (b0 + b) * kBoxK, m0, full_bar(it));
       }
     }
     __syncwarp();
@@ -231,9 +235,12 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
         const uint32_t st = base + static_cast<uint32_t>(s) * kStage;
         mbar_arrive_expect_tx(full_bar(s), nbi * (kWBox + kXBox));
         for (int b = 0; b < nbi; ++b)
-          tma_load_2d_hint(st + b * kWBox, &wmap, (b0 + b) * kBoxK, n0, full_bar(s), policy);
+          if (skg_check(st + (b + 1) * kWBox <= stages_end && ((b0 + b) * kBoxK) % 8 == 0, p.status,
+                        kCheckTmaW))
+            tma_load_2d_hint(st + b * kWBox, &wmap, (b0 + b) * kBoxK, n0, full_bar(s), policy);
         for (int b = 0; b < nbi; ++b)
-          tma_load_2d(st + NBOX * kWBox + b * kXBox, &xmap, (b0 + b) * kBoxK, m0, full_bar(s));
+          if (skg_check(st + NBOX * kWBox + (b + 1) * kXBox <= stages_end, p.status, kCheckTmaX))
+            tma_load_2d(st + NBOX * kWBox + b * kXBox, &xmap, (b0 + b) * kBoxK, m0, full_bar(s));
         if (dyn) next_b0 = static_cast<int>(atom_add_cluster_u32(counter, NBOX));
       }
       n_armed = it;
@@ -259,6 +266,9 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
         const uint32_t wst = base + static_cast<uint32_t>(s) * kStage;
         const uint32_t xst = wst + NBOX * kWBox;
         for (int b = 0; b < nbi; ++b) {
+          if (!skg_check(wst + (b + 1) * kWBox <= stages_end && xst + (b + 1) * kXBox <= stages_end,
+                         p.status, kCheckMmaOperand))
+            continue;
 #pragma unroll
           for (int j = 0; j < kBoxK / 16; ++j) {
             const uint64_t ad = sw128_kmajor_desc(wst + b * kWBox + j * 32);
@@ -297,7 +307,13 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
 #pragma unroll
     for (int c = 0; c < CH / 16; ++c) {
       float t16[16];
-      tmem_ld_32x32b_x16(row_taddr + static_cast<uint32_t>(c0 + c * 16), t16);
+      // (c0 and c are the same in every lane: the collective load stays warp-wide)
+      if (skg_check(c0 + c * 16 + 16 <= static_cast<int>(kTmemCols), p.status, kCheckTmem)) {
+        tmem_ld_32x32b_x16(row_taddr + static_cast<uint32_t>(c0 + c * 16), t16);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) t16[i] = 0.0f;
+      }
 #pragma unroll
       for (int i = 0; i < 16; ++i) v[c * 16 + i] = has_work ? t16[i] : 0.0f;
     }
@@ -329,7 +345,9 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
       load_chunk(c0, v);
 #pragma unroll
       for (int i = 0; i < CH; ++i)
-        if (row_ok && c0 + i < M)
+        if (row_ok && c0 + i < M &&
+            skg_check(dst >= base && dst + static_cast<uint32_t>((c0 + i) * RS + 1) * 4u <= smem_end,
+                      p.status, kCheckRedLocal))
           asm volatile("st.shared.f32 [%0], %1;" ::"r"(dst + static_cast<uint32_t>((c0 + i) * RS) * 4u),
                        "f"(v[i])
                        : "memory");
@@ -340,8 +358,10 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
       const uint32_t bytes = static_cast<uint32_t>(M * RS) * 4u;
       for (uint32_t j = 1; j < csize; ++j) {
         const uint32_t o = (rank + j) % csize;
-        bulk_copy_to_peer(mapa_shared(red + rank * blk, o), base + o * blk, bytes,
-                          mapa_shared(recv_bar, o));
+        if (skg_check(bytes <= blk && red + (rank + 1) * blk <= smem_end && base + (o + 1) * blk <= smem_end,
+                      p.status, kCheckBulk))
+          bulk_copy_to_peer(mapa_shared(red + rank * blk, o), base + o * blk, bytes,
+                            mapa_shared(recv_bar, o));
       }
     }
     if (!mbar_wait_bounded<true>(recv_bar, 0, p.timeout_ns))
@@ -362,6 +382,7 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
       for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
       for (uint32_t k = 0; k < csize; ++k) {
         const uint32_t a = red + k * blk + static_cast<uint32_t>(t * RS + rb * 8) * 4u;
+        if (!skg_check(a + 32u <= smem_end, p.status, kCheckRedRead)) continue;
         float4 q0, q1;
         asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
                      : "=f"(q0.x), "=f"(q0.y), "=f"(q0.z), "=f"(q0.w)
@@ -402,6 +423,9 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
       for (int g = 0; g < CH / 4; ++g) {
         const int gg = c0 / 4 + g;
         if (gg >= MG || !row_ok) continue;
+        if (!skg_check(owner < csize && red + row_off + (gg + 1) * 16u <= smem_end, p.status,
+                       owner == rank ? kCheckRedLocal : kCheckRedRemote))
+          continue;
         if (owner == rank)
           asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(red + row_off + gg * 16u),
                        "f"(v[4 * g]), "f"(v[4 * g + 1]), "f"(v[4 * g + 2]), "f"(v[4 * g + 3])
@@ -435,6 +459,10 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
       float acc[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+      if (!skg_check(red + static_cast<uint32_t>(((static_cast<int>(csize) - 1) * RS + rb * 8 + 7) * TP + t + 1) * 4u <=
+                         smem_end,
+                     p.status, kCheckRedRead))
+        continue;
       for (uint32_t k = 0; k < csize; ++k)
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[j] += redf[(k * RS + rb * 8 + j) * TP + t];

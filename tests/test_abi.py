@@ -37,6 +37,15 @@ def test_library_exports_every_declared_symbol(lib_path):
     assert not missing, f"declared but not exported: {missing}"
 
 
+def test_checked_library_exports_every_declared_symbol():
+    """The checked build (device-side bounds checks) is the same ABI."""
+    from skinny_bf16_projection_gb300 import build
+    _, checked = build.build_all()
+    lib = ctypes.CDLL(checked)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, f"declared but not exported by the checked build: {missing}"
+
+
 def test_binding_covers_the_header(lib_path):
     from skinny_bf16_projection_gb300 import _native
     bound = sorted(name for name, _, _ in _native.SIGNATURES)
