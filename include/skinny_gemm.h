@@ -287,6 +287,13 @@ int skinny_gemm_check_status(skinny_gemm_t h, void* stream);
  * setting the status word (no output is written).  count 0 clears it. */
 int skinny_gemm_debug_inject_timeout(skinny_gemm_t h, int count, uint64_t timeout_ns);
 
+/* Self-test of the checked build (libskinny_gemm_checked.so): the next `count`
+ * launches on this handle record one failed device check (access code 11) in
+ * the status word and return at once, without touching x or out, so that
+ * skinny_gemm_check_status reports SKG_ECHECK.  count 0 clears it.  EINVAL in
+ * the normal library, which has no device checks. */
+int skinny_gemm_debug_inject_check(skinny_gemm_t h, int count);
+
 /* Release the handle (its status word and staging buffers).  The caller must
  * make sure no launch using it is still pending.  NULL, an already destroyed
  * handle and a pointer that never was a handle are ignored.  Every entry point

@@ -172,6 +172,10 @@ class Projection:
     def inject_timeout(self, count: int, timeout_ns: int) -> None:
         _native.check(self._lib.skinny_gemm_debug_inject_timeout(self._h, count, timeout_ns))
 
+    def inject_check(self, count: int) -> None:
+        """Checked build only: the next `count` launches report one failed device check."""
+        _native.check(self._lib.skinny_gemm_debug_inject_check(self._h, count))
+
     # ---------------------------------------------------------------- lifetime
     def close(self) -> None:
         if getattr(self, "_h", None):

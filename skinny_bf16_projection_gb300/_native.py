@@ -40,6 +40,7 @@ SIGNATURES = [
     ("skinny_gemm_list_tactics", _int, [_vp, _i64, _cp, _sz]),
     ("skinny_gemm_check_status", _int, [_vp, _vp]),
     ("skinny_gemm_debug_inject_timeout", _int, [_vp, _int, _u64]),
+    ("skinny_gemm_debug_inject_check", _int, [_vp, _int]),
     ("skinny_gemm_run_noalloc", _int, [_vp, _i64, _i64, _i64, _int, _vp, _i64, _i64, _vp, _i64,
                                        _vp]),
     ("skinny_gemm_destroy", None, [_vp]),

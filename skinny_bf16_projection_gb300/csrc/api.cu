@@ -19,6 +19,11 @@
 #include "kernel_params.h"
 #include "skinny_gemm.h"
 
+// 1 in the checked build (libskinny_gemm_checked.so), whose kernels test their accesses.
+#ifndef SKG_DEVICE_CHECKS
+#define SKG_DEVICE_CHECKS 0
+#endif
+
 using namespace skg;
 
 // ------------------------------------------------------------------ errors
@@ -340,6 +345,7 @@ struct skinny_gemm_plan {
   void* out_stage = nullptr;
   uint64_t timeout_ns = 2000000000ull;
   int debug_count = 0;
+  int debug_kind = 1;  // KParams::debug_wait of the injected launches (1 timeout, 2 check)
   bool pdl = true;  // programmatic dependent launch attribute on every launch
   bool deterministic = false;  // the tuner keeps a fixed summation order (no :w tactics)
   uint64_t debug_timeout_ns = 0;
@@ -482,7 +488,7 @@ int launch_tactic(skinny_gemm_plan* h, const Tactic& t, const void* x, int64_t l
   p.red_stores = t.rs;
   if (h->debug_count > 0) {
     --h->debug_count;
-    p.debug_wait = 1;
+    p.debug_wait = h->debug_kind;
     p.timeout_ns = h->debug_timeout_ns;
   }
   cudaLaunchConfig_t cfg{};
@@ -1724,7 +1730,18 @@ int skinny_gemm_debug_inject_timeout(skinny_gemm_t h, int count, uint64_t timeou
   if (check_handle(h) != SKG_OK) return SKG_EINVAL;
   if (count < 0) return fail(SKG_EINVAL, "negative count");
   h->debug_count = count;
+  h->debug_kind = 1;
   h->debug_timeout_ns = timeout_ns;
+  return ok();
+}
+
+int skinny_gemm_debug_inject_check(skinny_gemm_t h, int count) {
+  if (check_handle(h) != SKG_OK) return SKG_EINVAL;
+  if (count < 0) return fail(SKG_EINVAL, "negative count");
+  if (SKG_DEVICE_CHECKS == 0)
+    return fail(SKG_EINVAL, "not a checked build (libskinny_gemm_checked.so has the device checks)");
+  h->debug_count = count;
+  h->debug_kind = 2;
   return ok();
 }
 

@@ -35,6 +35,7 @@ enum : uint32_t {
   kCheckOut = 8,        // output element inside [M, N]
   kCheckWorkspace = 9,  // stream-K partial-sum slot / tile counter
   kCheckBulk = 10,      // bulk DSMEM copy source / destination range
+  kCheckSelfTest = 11,  // injected by skinny_gemm_debug_inject_check (no access is made)
 };
 
 struct KParams {
@@ -46,7 +47,8 @@ struct KParams {
   int32_t stages;         // pipeline depth (shared-memory stages)
   uint32_t* status;       // device status word (watchdog)
   uint64_t timeout_ns;    // bound of every spin wait
-  int32_t debug_wait;     // nonzero: watchdog self-test, wait on a dead barrier and return
+  int32_t debug_wait;     // 1: watchdog self-test, wait on a dead barrier and return;
+                          // 2 (checked build): record a failed kCheckSelfTest and return
   int32_t pdl_late;       // 0: launch dependents right after the first stages' weight loads;
                           // k >= 1: only once all but the last k-1 stages' loads are issued
   int32_t red_alias;      // tcgen05 clusters: the reduction buffer reuses the pipeline stages

@@ -70,6 +70,11 @@ __global__ void __launch_bounds__(128) skinny_tc_kernel(const __grid_constant__ 
   const uint32_t lane = lane_id();
 
   if (p.debug_wait) {
+    // Checked-build self-test: one failed check, reported like a real one; no access.
+    if (p.debug_wait == 2) {
+      if (threadIdx.x == 0) skg_check(false, p.status, kCheckSelfTest);
+      return;
+    }
     // Watchdog self-test: wait on a barrier nothing will complete, report, return.
     if (threadIdx.x == 0) {
       mbar_init(dbg_bar, 1);

@@ -141,3 +141,39 @@ def test_overlap_step_checked(skg):
     for p in (main, fa, fb):
         p.check_status()
         p.close()
+
+
+def test_failed_check_is_reported_and_cleared(skg):
+    """The reporting path: an injected failed check (the checked build's
+    self-test, no access made) comes back from check_status as SKG_ECHECK naming
+    the access; the status is cleared and the next launch is correct."""
+    from skinny_bf16_projection_gb300 import _native
+    w, x, ref, s = full_case(656, 1088, seed=3)
+    proj = skg.Projection(w.to(DEV), use_tactic_file=False)
+    xd = x.to(DEV)
+    proj.inject_check(1)
+    run_proj(proj, xd[:4], torch.bfloat16)
+    with pytest.raises(skg.SkinnyGemmError) as e:
+        proj.check_status()
+    assert e.value.code == _native.SKG_ECHECK and "access 11" in str(e.value), str(e.value)
+    y = run_proj(proj, xd[:4], torch.bfloat16)
+    proj.check_status()
+    assert_parity(y, ref[:4], s[:4], "after the injected check")
+    proj.close()
+
+
+def test_normal_library_refuses_check_injection():
+    import __graft_entry__
+    __graft_entry__.build()
+    from skinny_bf16_projection_gb300 import _native, build
+    import skinny_bf16_projection_gb300 as m
+    lib = _native.load(build.LIB_PATH)
+    w = pin.weight(256, 512, seed=5).to(DEV)
+    h = lib.skinny_gemm_prepare(w.data_ptr(), 256, 512, _native.SKG_BF16, _native.SKG_BF16)
+    assert h
+    try:
+        assert lib.skinny_gemm_debug_inject_check(h, 1) == _native.SKG_EINVAL
+        assert b"not a checked build" in lib.skinny_gemm_last_error()
+    finally:
+        lib.skinny_gemm_destroy(h)
+    del m
