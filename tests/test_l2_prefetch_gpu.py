@@ -3,6 +3,8 @@
 what is computed, so every variant must match the oracle, and a dependent
 chain of projections (each output the next input) launched with it must give
 the bits of the same tactic launched without programmatic dependent launch."""
+import re
+
 import numpy as np
 import pytest
 import torch
@@ -74,7 +76,7 @@ def test_prefetch_dependent_chain_matches_no_pdl():
     no_pdl = skg().Projection(wd, use_tactic_file=False, pdl=False)
     links = 6
     for M in (1, 16, 32):
-        base = with_pdl.plan(M)
+        base = re.sub(r":p\d+", "", with_pdl.plan(M))  # the default plan may prefetch already
         no_pdl.set_tactic(M, base)
         ref = [x0[:M].to(DEV)] + [torch.empty((M, D), dtype=torch.bfloat16, device=DEV)
                                   for _ in range(links)]
