@@ -66,9 +66,23 @@ struct StageIter {
   }
 };
 
-// CTA owning unit u when U units are split over G CTAs as floor(c*U/G).
+// a / b for non-negative a, positive b: a 32-bit division when both fit (a
+// 64-bit one is a long dependent instruction sequence, and these sit on the
+// epilogue's critical path).
+__device__ __forceinline__ int64_t udiv_fast(int64_t a, int64_t b) {
+  if (((static_cast<uint64_t>(a) | static_cast<uint64_t>(b)) >> 32) == 0)
+    return static_cast<int64_t>(static_cast<uint32_t>(a) / static_cast<uint32_t>(b));
+  return a / b;
+}
+
+// First unit of CTA c when U units are split over G CTAs as floor(c*U/G).
+__device__ __forceinline__ int first_unit(int64_t c, int64_t U, int64_t G) {
+  return static_cast<int>(udiv_fast(c * U, G));
+}
+
+// CTA owning unit u under that split.
 __device__ __forceinline__ int cta_of_unit(int64_t u, int64_t U, int64_t G) {
-  return static_cast<int>(((u + 1) * G + U - 1) / U - 1);
+  return static_cast<int>(udiv_fast((u + 1) * G + U - 1, U) - 1);
 }
 
 }  // namespace
@@ -126,8 +140,8 @@ __global__ void __launch_bounds__(192) skinny_sk_kernel(const __grid_constant__ 
   const int64_t U = static_cast<int64_t>(ntiles) * kb;
   const int64_t G = gridDim.x;
   const int c = blockIdx.x;
-  const int u0 = static_cast<int>(c * U / G);
-  const int u1 = static_cast<int>((c + 1) * U / G);
+  const int u0 = first_unit(c, U, G);
+  const int u1 = first_unit(c + 1, U, G);
   const int first_tile = u0 / kb;
   const int M = p.M;
 
@@ -300,39 +314,42 @@ __global__ void __launch_bounds__(192) skinny_sk_kernel(const __grid_constant__ 
       named_barrier_sync(1, 128);
       if (*flag_g != 0u) {
         // Sum every part in CTA order (the same order whichever CTA arrives
-        // last).  Work items are (token, 4 consecutive rows); a thread keeps
-        // kIB items x kPB parts of loads in flight, then adds them in part
-        // order, so each batch costs one L2 round trip.
+        // last).  The parts are CTAs c_first..c_last; each wrote its slot
+        // 2 * cq, except c_first when its range began in the previous tile
+        // (then this tile is its second segment: slot 2 * cq + 1).  Work items
+        // are (token, 4 consecutive rows); a thread keeps kIB items x kPB
+        // parts of loads in flight, then adds them in part order, so each
+        // batch costs one L2 round trip.
         constexpr int kPB = 8;
-        constexpr int kIB = 4;
+        constexpr int kIB = 2;
         const int parts = c_last - c_first + 1;
+        const int first_slot =
+            2 * c_first + (first_unit(c_first, U, G) / kb == t ? 0 : 1);
         const int items = M * (ROWS / 4);
         for (int i0 = static_cast<int>(ep_tid); i0 < items; i0 += 128 * kIB) {
           float4 acc[kIB];
+          int off[kIB];
 #pragma unroll
-          for (int ii = 0; ii < kIB; ++ii) acc[ii] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          for (int ii = 0; ii < kIB; ++ii) {
+            acc[ii] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            const int item = i0 + ii * 128;
+            off[ii] = (item / (ROWS / 4)) * ROWS + (item % (ROWS / 4)) * 4;
+          }
           for (int q0 = 0; q0 < parts; q0 += kPB) {
-            const float* base_q[kPB];
-#pragma unroll
-            for (int q = 0; q < kPB; ++q) {
-              const int cq = c_first + min(q0 + q, parts - 1);
-              const int first_q = static_cast<int>(static_cast<int64_t>(cq) * U / G) / kb;
-              int slot = cq * 2 + (t == first_q ? 0 : 1);
-              if (!skg_check(slot >= 0 && slot < 2 * static_cast<int>(gridDim.x), p.status, kCheckWorkspace))
-                slot = 0;
-              base_q[q] = p.workspace + static_cast<int64_t>(slot) * TOK * ROWS;
-            }
             float4 pv[kIB][kPB];
 #pragma unroll
-            for (int ii = 0; ii < kIB; ++ii) {
-              const int item = i0 + ii * 128;
-              const int off = (item / (ROWS / 4)) * ROWS + (item % (ROWS / 4)) * 4;
+            for (int q = 0; q < kPB; ++q) {
+              const int slot = q0 + q == 0 ? first_slot : 2 * (c_first + q0 + q);
+              const bool slot_ok = q0 + q < parts &&
+                                   skg_check(slot >= 0 && slot < 2 * static_cast<int>(gridDim.x),
+                                             p.status, kCheckWorkspace);
+              const float* const part = p.workspace + static_cast<int64_t>(slot_ok ? slot : 0) * TOK * ROWS;
 #pragma unroll
-              for (int q = 0; q < kPB; ++q) {
+              for (int ii = 0; ii < kIB; ++ii) {
                 pv[ii][q] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                if (item < items && q0 + q < parts &&
-                    skg_check(off >= 0 && off + 4 <= TOK * ROWS, p.status, kCheckWorkspace))
-                  pv[ii][q] = ld_cg_f32x4(base_q[q] + off);
+                if (slot_ok && i0 + ii * 128 < items &&
+                    skg_check(off[ii] >= 0 && off[ii] + 4 <= TOK * ROWS, p.status, kCheckWorkspace))
+                  pv[ii][q] = __ldcg(reinterpret_cast<const float4*>(part + off[ii]));
               }
             }
 #pragma unroll
