@@ -803,6 +803,19 @@ def main():
     done[(e2e_steps - 1) % 2].synchronize()
     e2e_s = reduce_max(time.perf_counter() - t0, world) / e2e_steps
     e2e_two_streams = world * n_launch * wbytes / e2e_s / 1e9
+    # Every step above copied its results back: those of the last two steps (one
+    # per buffer set) must be the device path's (bit for bit with a fixed-order
+    # plan, else within bf16 rounding of it).
+    e2e_checked = True
+    for M in SWEEP:
+        ref = outs[M].float().cpu()
+        for host in (oh[M], oh_b[M]):
+            if ":w" in plan[M]:
+                e2e_checked &= bool(torch.allclose(host.float(), ref, rtol=2e-2, atol=2e-3))
+            else:
+                e2e_checked &= bool(torch.equal(host, outs[M].cpu()))
+    if not e2e_checked:
+        raise RuntimeError("end-to-end outputs differ from the device path's")
     # The same step with the copies batched around the projections on one stream:
     # every x (packed in one pinned host buffer, one row block per projection) copied
     # in with one copy, the skinny_gemm_run calls back to back (so programmatic
@@ -906,6 +919,7 @@ def main():
                 "h2d_bytes_per_step": sum(M * K_DEC * 2 for M in SWEEP),
                 "d2h_bytes_per_step": sum(M * N_DEC * 2 for M in SWEEP),
                 "method": e2e_method,
+                "outputs_match_device_path": e2e_checked,
                 "batched_copies_value": round(e2e_batched, 2),
                 "host_async_graph_value": round(e2e_async, 2),
                 "host_async_graph_two_in_flight_value": round(e2e_pipelined, 2),
