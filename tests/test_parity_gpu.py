@@ -417,6 +417,27 @@ def test_stream_k_every_tactic_full_size(N):
         proj.check_status()
 
 
+def test_stream_k_ctas_spanning_several_tiles():
+    """A short K (4 boxes per row tile) over 313 row tiles, the last one ragged:
+    with one or two CTAs per SM a stream-K CTA covers 4-9 boxes, so it can hold
+    whole tiles between its first and last split ones, and a split tile's first
+    part can be the last segment of a CTA that began in an earlier tile."""
+    N, K = 40000, 256
+    w, x, ref, s = full_case(N, K, seed=4)
+    xd = x.to(DEV)
+    proj = skg().Projection(w.to(DEV), use_tactic_file=False)
+    n = 0
+    for M in (1, 16, 64):
+        for t in [t for t in proj.tactics(M) if t.startswith("sk:")]:
+            proj.set_tactic(M, t)
+            for _ in range(2):  # twice: the tile counters must be back at zero
+                y = run_proj(proj, xd[:M], torch.bfloat16)
+                assert_parity(y, ref[:M], s[:M], f"N={N} K={K} M={M} {t}")
+            n += 1
+    proj.check_status()
+    assert n >= 6, n
+
+
 def test_dependent_chain_without_pdl_matches_with_pdl():
     """The same 8-link dependent chain launched without programmatic dependent
     launch gives the same bits as with it."""
